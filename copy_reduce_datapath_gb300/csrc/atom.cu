@@ -1,0 +1,522 @@
+// The Atom datapath and the device side of SNAC for sm_103a.
+//
+// "Purlin: Separating Orchestration from the Datapath of Collectives":
+//   - abstract: the Atom provides the two data-movement primitives of
+//     collectives, copy and reduce; SNAC (Stage, Notify, And Consume) is the
+//     orchestration above it;
+//   - Table 1 ("Compatibility"): a datapath built on vectorised loads and
+//     stores; Figure 11 caption: a pipelined copy with 1 to 8 stages.
+//
+// One persistent kernel executes a work list (see snac.h).  Every work item
+// is "wait on flags -> move -> notify / credit flags", and the move is either
+// a copy of one source into up to 64 destinations or the fp32 sum, in rank
+// order, of up to 64 sources written to up to 64 destinations.  Items are
+// claimed in index order (a device counter) whenever an item waits on another,
+// so a waiting CTA only ever waits for items that were claimed before it and
+// are therefore running: the grid makes progress without co-residency.  Every
+// wait is bounded by a timeout on %globaltimer and an iteration cap; a wait
+// that gives up records PL_ERR_TIMEOUT in the status word and raises an abort
+// flag that makes every other wait give up too, so the kernel always returns.
+#include "snac.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace purlin {
+namespace {
+
+constexpr int kStatusTimeout = 6;  // PL_ERR_TIMEOUT
+constexpr int kCtasPerSm = 1;
+
+// ------------------------------------------------------- memory-model helpers
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v)
+{
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(unsigned int* p, unsigned int v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Streaming 16-byte load that is served from L2 (data may have been written
+// by another CTA of this launch after a flag acquire).
+__device__ __forceinline__ uint4 ld16(const char* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void st16(char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// ------------------------------------------------------------- bounded waits
+
+__device__ void give_up(const LaunchArgs& a)
+{
+    atomicCAS(a.st.status, 0, kStatusTimeout);
+    atomicExch(a.st.abort, 1);
+}
+
+// Waits until *flag >= target.  false: the wait expired or another wait did.
+__device__ bool wait_at_least(const unsigned long long* flag, unsigned long long target, const LaunchArgs& a)
+{
+    const unsigned long long t0 = global_ns();
+    // The cap bounds the loop even if %globaltimer stalled: every iteration
+    // sleeps, and 2^26 iterations exceed any sensible timeout.
+    const unsigned int cap = 1u << 26;
+    for (unsigned int it = 0; it < cap; ++it) {
+        if (ld_acquire(flag) >= target)
+            return true;
+        if ((it & 31) == 31) {
+            if (ld_relaxed_s32(a.st.abort))
+                return false;
+            if (global_ns() - t0 > a.timeout_ns)
+                break;
+        }
+        __nanosleep(it < 64 ? 32 : 256);
+    }
+    give_up(a);
+    return false;
+}
+
+__device__ __forceinline__ unsigned long long tag(const LaunchArgs& a, unsigned int use)
+{
+    return (a.epoch << 24) | (unsigned long long)(use + 1u);
+}
+
+// Thread 0 of the CTA: every wait of the item.
+__device__ bool run_waits(const LaunchArgs& a, const Item& it)
+{
+    if (ld_relaxed_s32(a.st.abort))
+        return false;
+    for (unsigned k = 0; k < it.nwait; ++k) {
+        const Sync s = a.syncs[it.sync + k];
+        const unsigned long long* f = s.type == kWaitFull ? a.st.full + s.flag : a.st.done + s.flag;
+        if (!wait_at_least(f, tag(a, s.use), a))
+            return false;
+    }
+    return true;
+}
+
+// Thread 0 of the CTA, after a barrier that follows the item's stores.
+__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index)
+{
+    __threadfence();
+    for (unsigned k = it.nwait; k < (unsigned)it.nwait + it.npost; ++k) {
+        const Sync s = a.syncs[it.sync + k];
+        if (s.type == kNotify) {
+            if ((long long)index == a.drop_notify)
+                continue;  // test hook: consumers of this item will time out
+            st_release(a.st.full + s.flag, tag(a, s.use));
+        } else if (s.type == kCredit) {
+            unsigned old = atom_add_acq_rel(a.st.count + s.flag, 1u);
+            if (old + 1u == s.count) {
+                st_relaxed_u32(a.st.count + s.flag, 0u);
+                st_release(a.st.done + s.flag, tag(a, s.use));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- element math
+
+template <int S> struct Elem;
+
+template <> struct Elem<2> {  // bf16
+    static __device__ __forceinline__ float to_f(uint32_t h) { return __uint_as_float(h << 16); }
+    static __device__ __forceinline__ uint32_t from_f(float f)
+    {
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+    static __device__ __forceinline__ uint32_t load(const char* p) { return __ldcg(reinterpret_cast<const unsigned short*>(p)); }
+    static __device__ __forceinline__ void store(char* p, uint32_t v) { *reinterpret_cast<unsigned short*>(p) = (unsigned short)v; }
+};
+
+template <> struct Elem<4> {  // fp32
+    static __device__ __forceinline__ float to_f(uint32_t w) { return __uint_as_float(w); }
+    static __device__ __forceinline__ uint32_t from_f(float f) { return __float_as_uint(f); }
+    static __device__ __forceinline__ uint32_t load(const char* p) { return __ldcg(reinterpret_cast<const unsigned int*>(p)); }
+    static __device__ __forceinline__ void store(char* p, uint32_t v) { *reinterpret_cast<unsigned int*>(p) = v; }
+};
+
+// Accumulators of one 16-byte vector: 8 bf16 or 4 fp32 lanes.
+template <int S> struct Acc {
+    static constexpr int N = 16 / S;
+    float v[N];
+    __device__ __forceinline__ void set(uint4 x)
+    {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (S == 2) {
+                v[2 * i] = Elem<2>::to_f(w[i] & 0xFFFFu);
+                v[2 * i + 1] = Elem<2>::to_f(w[i] >> 16);
+            } else {
+                v[i] = Elem<4>::to_f(w[i]);
+            }
+        }
+    }
+    __device__ __forceinline__ void add(uint4 x)
+    {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (S == 2) {
+                v[2 * i] = __fadd_rn(v[2 * i], Elem<2>::to_f(w[i] & 0xFFFFu));
+                v[2 * i + 1] = __fadd_rn(v[2 * i + 1], Elem<2>::to_f(w[i] >> 16));
+            } else {
+                v[i] = __fadd_rn(v[i], Elem<4>::to_f(w[i]));
+            }
+        }
+    }
+    __device__ __forceinline__ uint4 pack() const
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (S == 2)
+                w[i] = Elem<2>::from_f(v[2 * i]) | (Elem<2>::from_f(v[2 * i + 1]) << 16);
+            else
+                w[i] = Elem<4>::from_f(v[i]);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// The 16 bytes that start q bytes into the 32-byte pair (lo, hi); q is even.
+__device__ __forceinline__ uint4 realign(uint4 lo, uint4 hi, int q)
+{
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const int k = q >> 2;
+    const unsigned sh = (unsigned)(q & 3) * 8u;
+    uint32_t r[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t a0 = k == 0 ? w[m] : k == 1 ? w[m + 1] : k == 2 ? w[m + 2] : w[m + 3];
+        const uint32_t a1 = k == 0 ? w[m + 1] : k == 1 ? w[m + 2] : k == 2 ? w[m + 3] : w[m + 4];
+        r[m] = __funnelshift_r(a0, a1, sh);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// ------------------------------------------------------------ the datapath
+
+// Per-item shared state: byte pointers of row 0 and byte strides between rows.
+struct ItemShared {
+    const char* src[kMaxRanks];
+    char* dst[kMaxRanks];
+    unsigned long long sstride[kMaxRanks];
+    unsigned long long dstride[kMaxRanks];
+};
+
+// Row pointer of source s / destination d.
+#define SRC_ROW(sh, s, row) ((sh).src[s] + (size_t)(row) * (sh).sstride[s])
+#define DST_ROW(sh, d, row) ((sh).dst[d] + (size_t)(row) * (sh).dstride[d])
+
+// Copy of nv 16-byte vectors from one source to every destination in `mask`.
+// The destinations are 16-byte aligned at `body`; the source is `q` bytes past
+// a 16-byte boundary (QALIGNED: q == 0).  U vectors in flight per thread.
+template <bool QALIGNED>
+__device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
+                                       unsigned nv, int tid, int nthr)
+{
+    constexpr int U = QALIGNED ? 8 : 4;
+    const char* src = SRC_ROW(sh, 0, row) + body;
+    const int q = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
+    const char* base = src - q;
+    const unsigned step = (unsigned)nthr * U;
+    for (unsigned v0 = tid; v0 < nv; v0 += step) {
+        uint4 x[U];
+        if constexpr (QALIGNED) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
+                if (v < nv)
+                    x[u] = ld16(base + (size_t)v * 16);
+            }
+        } else {
+            uint4 lo[U], hi[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
+                if (v < nv) {
+                    lo[u] = ld16(base + (size_t)v * 16);
+                    hi[u] = ld16(base + (size_t)v * 16 + 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                x[u] = realign(lo[u], hi[u], q);
+        }
+#pragma unroll 1
+        for (unsigned long long m = mask; m; m &= m - 1) {
+            const int d = __ffsll((long long)m) - 1;
+            char* dst = DST_ROW(sh, d, row) + body;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
+                if (v < nv)
+                    st16(dst + (size_t)v * 16, x[u]);
+            }
+        }
+    }
+}
+
+// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
+// to every destination in `mask`.  G sources in flight per thread.
+template <int S, bool QALIGNED>
+__device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                      size_t body, unsigned nv, int tid, int nthr)
+{
+    constexpr int G = QALIGNED ? 8 : 4;
+    for (unsigned v = tid; v < nv; v += nthr) {
+        Acc<S> acc;
+        for (int s0 = 0; s0 < nsrc; s0 += G) {
+            uint4 x[G];
+            if constexpr (QALIGNED) {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (s0 + g < nsrc)
+                        x[g] = ld16(SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16);
+            } else {
+                uint4 lo[G], hi[G];
+                int q[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (s0 + g < nsrc) {
+                        const char* p = SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16;
+                        q[g] = (int)(reinterpret_cast<uintptr_t>(p) & 15u);
+                        lo[g] = ld16(p - q[g]);
+                        hi[g] = q[g] ? ld16(p - q[g] + 16) : lo[g];
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (s0 + g < nsrc)
+                        x[g] = q[g] ? realign(lo[g], hi[g], q[g]) : lo[g];
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if (s0 + g < nsrc) {
+                    if (s0 + g == 0)
+                        acc.set(x[g]);
+                    else
+                        acc.add(x[g]);
+                }
+            }
+        }
+        const uint4 out = acc.pack();
+#pragma unroll 1
+        for (unsigned long long m = mask; m; m &= m - 1) {
+            const int d = __ffsll((long long)m) - 1;
+            st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, out);
+        }
+    }
+}
+
+// One row segment of n elements, executed by `nthr` threads with index `tid`.
+// Destinations in `mask` share the same address mod 16 (`dcls`); their
+// stores are 16-byte aligned after a head of at most 16/S - 1 elements, and
+// the rest up to the last whole vector goes through the vector bodies.
+template <int S, int OPS>
+__device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                     unsigned n, unsigned dcls, int tid, int nthr)
+{
+    constexpr int E = 16 / S;
+    unsigned head = ((16u - dcls) & 15u) / S;
+    if (head > n)
+        head = n;
+    const unsigned nv = (n - head) / E;
+    const unsigned tail0 = head + nv * E;
+    const unsigned ntail = n - tail0;
+
+    // Scalar head and tail elements.
+    for (unsigned e = tid; e < head + ntail; e += nthr) {
+        const unsigned i = e < head ? e : tail0 + (e - head);
+        uint32_t v;
+        if (nsrc == 1) {
+            v = Elem<S>::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
+        } else {
+            float acc = Elem<S>::to_f(Elem<S>::load(SRC_ROW(sh, 0, row) + (size_t)i * S));
+#pragma unroll 1
+            for (int s = 1; s < nsrc; ++s)
+                acc = __fadd_rn(acc, Elem<S>::to_f(Elem<S>::load(SRC_ROW(sh, s, row) + (size_t)i * S)));
+            v = Elem<S>::from_f(acc);
+        }
+#pragma unroll 1
+        for (unsigned long long m = mask; m; m &= m - 1) {
+            const int d = __ffsll((long long)m) - 1;
+            Elem<S>::store(DST_ROW(sh, d, row) + (size_t)i * S, v);
+        }
+    }
+    if (nv == 0)
+        return;
+
+    const size_t body = (size_t)head * S;
+    bool aligned = true;
+    for (int s = 0; s < nsrc; ++s)
+        aligned &= ((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == 0;
+    if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1)) {
+        if (aligned)
+            copy_body<true>(sh, mask, row, body, nv, tid, nthr);
+        else
+            copy_body<false>(sh, mask, row, body, nv, tid, nthr);
+    } else if (OPS & kOpsSum) {
+        if (aligned)
+            sum_body<S, true>(sh, nsrc, mask, row, body, nv, tid, nthr);
+        else
+            sum_body<S, false>(sh, nsrc, mask, row, body, nv, tid, nthr);
+    }
+}
+
+// Moves one rows x cols block.  A one-row block is spread over the whole CTA;
+// a multi-row block gives each warp whole rows.  Destinations are grouped by
+// address mod 16; each group is one pass over the sources.
+template <int S, int OPS>
+__device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
+                                          unsigned long long cols)
+{
+    const bool one_row = rows == 1;
+    const int tid = one_row ? (int)threadIdx.x : (int)(threadIdx.x & 31);
+    const int nthr = one_row ? (int)blockDim.x : 32;
+    const unsigned r0 = one_row ? 0u : threadIdx.x >> 5;
+    const unsigned rstep = one_row ? 1u : blockDim.x >> 5;
+    for (unsigned r = r0; r < rows; r += rstep) {
+        unsigned long long todo = ndst >= 64 ? ~0ull : ((1ull << ndst) - 1ull);
+        while (todo) {
+            const int d0 = __ffsll((long long)todo) - 1;
+            const unsigned cls = (unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d0, r)) & 15u);
+            unsigned long long group = 0;
+            for (unsigned long long m = todo; m; m &= m - 1) {
+                const int d = __ffsll((long long)m) - 1;
+                if ((unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d, r)) & 15u) == cls)
+                    group |= 1ull << d;
+            }
+            todo &= ~group;
+            segment<S, OPS>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr);
+        }
+    }
+}
+
+// ------------------------------------------------------------- the kernel
+
+template <int S, int OPS>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid_constant__ LaunchArgs a)
+{
+    __shared__ ItemShared sh;
+    __shared__ unsigned s_index;
+    __shared__ int s_ok;
+    __shared__ Item s_item;
+    const int tid = (int)threadIdx.x;
+
+    for (unsigned k = 0;; ++k) {
+        if (tid == 0) {
+            s_index = a.use_tickets ? atomicAdd(a.st.ticket, 1u) : blockIdx.x + k * gridDim.x;
+            if (s_index < a.nitems)
+                s_item = a.items[s_index];
+        }
+        __syncthreads();
+        const unsigned index = s_index;
+        if (index >= a.nitems)
+            break;
+        const Item it = s_item;
+        const int nref = it.nsrc + it.ndst;
+        if (tid < nref) {
+            const Ref f = a.refs[it.ref + tid];
+            char* base = a.bufs[f.buf] + f.offset * (unsigned long long)S;
+            const unsigned long long stride = f.stride * (unsigned long long)S;
+            if (tid < it.nsrc) {
+                sh.src[tid] = base;
+                sh.sstride[tid] = stride;
+            } else {
+                sh.dst[tid - it.nsrc] = base;
+                sh.dstride[tid - it.nsrc] = stride;
+            }
+        }
+        if (tid == 0)
+            s_ok = it.nwait ? run_waits(a, it) : 1;
+        __syncthreads();
+        if (s_ok)
+            move_item<S, OPS>(sh, it.nsrc, it.ndst, it.rows, it.cols);
+        __syncthreads();
+        if (tid == 0 && s_ok && it.npost)
+            run_posts(a, it, index);
+    }
+
+    if (a.use_tickets && tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.st.exited, 1u) == gridDim.x - 1) {
+            // Last CTA out: every other CTA has taken its final ticket.
+            *a.st.ticket = 0u;
+            *a.st.exited = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream)
+{
+    (void)bulk;
+    (void)stages;
+    const int ops = args.ops;
+#define PL_LAUNCH(SZ, OPS) snac_kernel<SZ, OPS><<<ctas, kThreads, 0, stream>>>(args)
+    if (args.dtype == 0) {
+        if (ops == kOpsCopy)
+            PL_LAUNCH(2, kOpsCopy);
+        else if (ops == kOpsSum)
+            PL_LAUNCH(2, kOpsSum);
+        else
+            PL_LAUNCH(2, kOpsCopy | kOpsSum);
+    } else {
+        if (ops == kOpsCopy)
+            PL_LAUNCH(4, kOpsCopy);
+        else if (ops == kOpsSum)
+            PL_LAUNCH(4, kOpsSum);
+        else
+            PL_LAUNCH(4, kOpsCopy | kOpsSum);
+    }
+#undef PL_LAUNCH
+    return cudaGetLastError();
+}
+
+int snac_ctas_per_sm(bool bulk, int stages)
+{
+    (void)bulk;
+    (void)stages;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum>, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace purlin

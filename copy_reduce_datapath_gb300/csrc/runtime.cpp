@@ -1,0 +1,1324 @@
+// Host runtime of libpurlin1: layouts, validation, the SNAC derivation of a
+// work list from a layout pair, the per-context work-list cache and the launch
+// of the persistent Atom kernel.
+//
+// "Purlin: Separating Orchestration from the Datapath of Collectives":
+//   - abstract: collectives are specified as (input layout, output layout,
+//     copy or reduction); SNAC derives coordination from that specification;
+//   - Table 1 ("Derivability"): no explicit communication schedule is written
+//     by hand -- here every work item, flag and ring slot comes from the
+//     layout pair alone;
+//   - Figure 6 caption: chunks are staged incrementally and the AllReduce
+//     owner reduces its partition while the other ranks gather reduced chunks;
+//   - Figure 10 caption: Purlin-ZS omits staging.
+#include "purlin.h"
+#include "snac.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <new>
+#include <string>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+using namespace purlin;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr uint64_t kMinChunkBytes = 8 << 10;
+constexpr uint64_t kMaxChunkBytes = 4 << 20;
+constexpr int kItemsPerCta = 4;       // auto chunking aims at this many items per CTA
+constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threads x 128 registers)
+constexpr size_t kMaxCachedPlans = 1024;
+constexpr uint32_t kMaxUsesPerLaunch = (1u << 24) - 2;
+
+uint64_t elem_size(pl_dtype dt) { return dt == PL_BF16 ? 2 : 4; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ layouts
+
+struct pl_layout {
+    int R = 0;
+    std::vector<int> first;      // R + 1 prefix counts into parts
+    std::vector<pl_part> parts;  // contiguous regions normalised to rows = 1
+};
+
+namespace {
+
+bool mul_overflows(uint64_t a, uint64_t b) { return a != 0 && b > UINT64_MAX / a; }
+
+// Last element index + 1 of a region.
+uint64_t region_extent(const pl_part& p)
+{
+    if (p.len == 0)
+        return p.offset;
+    return p.offset + (p.rows - 1) * p.row_stride + p.len;
+}
+
+uint64_t region_count(const pl_part& p) { return p.rows * p.len; }
+
+pl_status make_layout(pl_layout** out, int R, const std::vector<int>& counts, const std::vector<pl_part>& parts)
+{
+    if (!out || R < 1 || R > kMaxRanks || (int)counts.size() != R)
+        return PL_ERR_INVALID;
+    std::unique_ptr<pl_layout> L(new (std::nothrow) pl_layout);
+    if (!L)
+        return PL_ERR_NOMEM;
+    L->R = R;
+    L->first.assign(R + 1, 0);
+    size_t total = 0;
+    for (int r = 0; r < R; ++r) {
+        if (counts[r] < 0)
+            return PL_ERR_INVALID;
+        total += (size_t)counts[r];
+        L->first[r + 1] = (int)total;
+    }
+    if (total != parts.size())
+        return PL_ERR_INVALID;
+    L->parts.reserve(total);
+    for (pl_part p : parts) {
+        if (p.rows == 0)
+            return PL_ERR_INVALID;
+        if (p.rows > 1 && p.row_stride < p.len)
+            return PL_ERR_INVALID;
+        if (mul_overflows(p.rows, p.len) || p.rows * p.len > (1ull << 56))
+            return PL_ERR_INVALID;
+        if (p.rows > 1 && (mul_overflows(p.rows - 1, p.row_stride) || (p.rows - 1) * p.row_stride > (1ull << 58)))
+            return PL_ERR_INVALID;
+        if (p.offset > (1ull << 58))
+            return PL_ERR_INVALID;
+        // A region whose rows touch end to end is contiguous: one row of rows*len.
+        if (p.rows == 1 || p.row_stride == p.len) {
+            p.len = p.rows * p.len;
+            p.rows = 1;
+            p.row_stride = p.len;
+        }
+        L->parts.push_back(p);
+    }
+    *out = L.release();
+    return PL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PL_API int pl_abi_version(void) { return PL_ABI_VERSION; }
+
+PL_API const char* pl_status_str(pl_status s)
+{
+    switch (s) {
+    case PL_OK: return "ok";
+    case PL_ERR_INVALID: return "invalid argument";
+    case PL_ERR_LAYOUT: return "the layout pair does not name a valid collective for these buffers";
+    case PL_ERR_ALIAS: return "an output overlaps another output or an input it may not alias";
+    case PL_ERR_NOMEM: return "out of device memory, or scratch ring too small for the staged path";
+    case PL_ERR_CUDA: return "a CUDA call failed";
+    case PL_ERR_TIMEOUT: return "a bounded device wait expired";
+    case PL_ERR_UNSUPPORTED: return "layout pair not supported by this datapath";
+    default: return "unknown status";
+    }
+}
+
+PL_API void pl_policy_default(pl_policy* pol)
+{
+    if (!pol)
+        return;
+    std::memset(pol, 0, sizeof *pol);
+    pol->debug_drop_notify = -1;
+}
+
+PL_API pl_status pl_layout_create(pl_layout** layout, int R, const int* nparts, const pl_part* parts)
+{
+    if (!layout || !nparts || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(nparts, nparts + R);
+    size_t total = 0;
+    for (int c : counts) {
+        if (c < 0)
+            return PL_ERR_INVALID;
+        total += (size_t)c;
+    }
+    if (total && !parts)
+        return PL_ERR_INVALID;
+    std::vector<pl_part> v(parts, parts + total);
+    return make_layout(layout, R, counts, v);
+}
+
+PL_API pl_status pl_layout_destroy(pl_layout* layout)
+{
+    delete layout;
+    return PL_OK;
+}
+
+PL_API pl_status pl_layout_info(const pl_layout* layout, int* R, int* total_parts)
+{
+    if (!layout)
+        return PL_ERR_INVALID;
+    if (R)
+        *R = layout->R;
+    if (total_parts)
+        *total_parts = (int)layout->parts.size();
+    return PL_OK;
+}
+
+PL_API pl_status pl_layout_rank_owned(pl_layout** layout, int R, const uint64_t* lens)
+{
+    if (!lens || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(R, 1);
+    std::vector<pl_part> parts;
+    for (int k = 0; k < R; ++k)
+        parts.push_back(pl_part{(uint64_t)k, 0, lens[k], 1, lens[k]});
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_partitioned(pl_layout** layout, int R, const uint64_t* lens)
+{
+    if (!lens || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(R, R);
+    std::vector<pl_part> parts;
+    for (int r = 0; r < R; ++r) {
+        uint64_t o = 0;
+        for (int k = 0; k < R; ++k) {
+            parts.push_back(pl_part{(uint64_t)k, o, lens[k], 1, lens[k]});
+            o += lens[k];
+        }
+    }
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_rank_owned_inplace(pl_layout** layout, int R, const uint64_t* lens)
+{
+    if (!lens || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(R, 1);
+    std::vector<pl_part> parts;
+    uint64_t o = 0;
+    for (int k = 0; k < R; ++k) {
+        parts.push_back(pl_part{(uint64_t)k, o, lens[k], 1, lens[k]});
+        o += lens[k];
+    }
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_alltoall_in(pl_layout** layout, int R, const uint64_t* m)
+{
+    if (!m || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(R, R);
+    std::vector<pl_part> parts;
+    for (int r = 0; r < R; ++r) {
+        uint64_t o = 0;
+        for (int j = 0; j < R; ++j) {
+            uint64_t n = m[(size_t)r * R + j];
+            parts.push_back(pl_part{(uint64_t)r * R + j, o, n, 1, n});
+            o += n;
+        }
+    }
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_alltoall_out(pl_layout** layout, int R, const uint64_t* m)
+{
+    if (!m || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    std::vector<int> counts(R, R);
+    std::vector<pl_part> parts;
+    for (int j = 0; j < R; ++j) {
+        uint64_t o = 0;
+        for (int r = 0; r < R; ++r) {
+            uint64_t n = m[(size_t)r * R + j];
+            parts.push_back(pl_part{(uint64_t)r * R + j, o, n, 1, n});
+            o += n;
+        }
+    }
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_ulysses_in(pl_layout** layout, int R, uint64_t S, uint64_t H, uint64_t D)
+{
+    if (R < 1 || R > kMaxRanks || H % (uint64_t)R)
+        return PL_ERR_INVALID;
+    uint64_t hs = H / (uint64_t)R;
+    std::vector<int> counts(R, R);
+    std::vector<pl_part> parts;
+    for (int r = 0; r < R; ++r)
+        for (int j = 0; j < R; ++j)
+            parts.push_back(pl_part{(uint64_t)r * R + j, (uint64_t)j * hs * D, hs * D, S ? S : 1, H * D});
+    if (S == 0)
+        for (auto& p : parts)
+            p.len = 0;
+    return make_layout(layout, R, counts, parts);
+}
+
+PL_API pl_status pl_layout_ulysses_out(pl_layout** layout, int R, uint64_t S, uint64_t H, uint64_t D)
+{
+    if (R < 1 || R > kMaxRanks || H % (uint64_t)R)
+        return PL_ERR_INVALID;
+    uint64_t blk = S * (H / (uint64_t)R) * D;
+    std::vector<int> counts(R, R);
+    std::vector<pl_part> parts;
+    for (int j = 0; j < R; ++j)
+        for (int r = 0; r < R; ++r)
+            parts.push_back(pl_part{(uint64_t)r * R + j, (uint64_t)r * blk, blk, 1, blk});
+    return make_layout(layout, R, counts, parts);
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------- derivation
+
+namespace {
+
+struct Region {
+    int space;  // PL_SPACE_IN / PL_SPACE_OUT
+    int rank;
+    uint64_t offset, rows, cols, stride;
+};
+
+// All regions of one name: the transfer the name asks for.
+struct Transfer {
+    uint64_t name;
+    std::vector<Region> srcs;  // rank order
+    std::vector<Region> dsts;  // rank order
+    uint64_t count;
+};
+
+struct Chunk {
+    uint64_t row0, nrows, col0, ncols;
+};
+
+struct ResolvedPolicy {
+    int path;       // PL_PATH_ZS / PL_PATH_STAGED
+    int ar_form;    // PL_AR_FUSED / PL_AR_COMPOSED
+    int datapath;   // PL_ATOM_VECTOR / PL_ATOM_BULK
+    int ctas;       // 0 = auto
+    int stages;
+    uint64_t chunk_bytes;
+    uint64_t timeout_ns;
+    int64_t drop_notify;
+};
+
+pl_status resolve_policy(const pl_policy* p, ResolvedPolicy& rp)
+{
+    pl_policy d;
+    pl_policy_default(&d);
+    if (!p)
+        p = &d;
+    if (p->path < PL_PATH_AUTO || p->path > PL_PATH_STAGED)
+        return PL_ERR_INVALID;
+    if (p->allreduce_form < PL_AR_AUTO || p->allreduce_form > PL_AR_COMPOSED)
+        return PL_ERR_INVALID;
+    if (p->datapath < PL_ATOM_AUTO || p->datapath > PL_ATOM_BULK)
+        return PL_ERR_INVALID;
+    if (p->ctas < 0 || p->stages < 0 || p->stages > kBulkMaxStages)
+        return PL_ERR_INVALID;
+    rp.path = p->path == PL_PATH_AUTO ? PL_PATH_ZS : p->path;
+    rp.ar_form = p->allreduce_form == PL_AR_AUTO ? PL_AR_FUSED : p->allreduce_form;
+    rp.datapath = p->datapath == PL_ATOM_AUTO ? PL_ATOM_VECTOR : p->datapath;
+    rp.ctas = p->ctas;
+    rp.stages = p->stages ? p->stages : 4;
+    // Work items address columns with 32-bit counts: keep chunks well below 2^32 elements.
+    rp.chunk_bytes = p->chunk_bytes ? std::min<uint64_t>(std::max<uint64_t>(p->chunk_bytes, 256), 1ull << 30) : 0;
+    rp.timeout_ns = p->poll_timeout_ns ? p->poll_timeout_ns : kDefaultTimeoutNs;
+    rp.drop_notify = p->debug_drop_notify;
+    return PL_OK;
+}
+
+struct HostPlan {
+    int R = 0;
+    pl_dtype dtype = PL_BF16;
+    std::vector<Item> items;
+    std::vector<Ref> refs;
+    std::vector<Sync> syncs;
+    uint32_t nflags = 0;
+    int ops = 0;  // kOpsCopy | kOpsSum
+    pl_plan_stats stats{};
+};
+
+pl_status collect_transfers(const pl_layout& in, const pl_layout& out, pl_op op, int R,
+                            std::vector<Transfer>& ts)
+{
+    std::unordered_map<uint64_t, std::vector<std::pair<int, int>>> by_name;
+    for (int r = 0; r < R; ++r)
+        for (int i = in.first[r]; i < in.first[r + 1]; ++i)
+            by_name[in.parts[i].name].push_back({r, i});
+    std::unordered_map<uint64_t, size_t> index;
+    for (int r = 0; r < R; ++r) {
+        for (int i = out.first[r]; i < out.first[r + 1]; ++i) {
+            const pl_part& p = out.parts[i];
+            auto it = index.find(p.name);
+            if (it == index.end()) {
+                index[p.name] = ts.size();
+                Transfer t;
+                t.name = p.name;
+                t.count = region_count(p);
+                ts.push_back(t);
+                it = index.find(p.name);
+            }
+            Transfer& t = ts[it->second];
+            if (region_count(p) != t.count)
+                return PL_ERR_LAYOUT;
+            t.dsts.push_back(Region{PL_SPACE_OUT, r, p.offset, p.rows, p.len, p.row_stride});
+        }
+    }
+    for (Transfer& t : ts) {
+        auto it = by_name.find(t.name);
+        if (it == by_name.end())
+            return PL_ERR_LAYOUT;
+        const auto& srcs = it->second;
+        if (op == PL_COPY) {
+            if (srcs.size() != 1)
+                return PL_ERR_LAYOUT;
+        } else {
+            if ((int)srcs.size() != R)
+                return PL_ERR_LAYOUT;
+            for (int r = 0; r < R; ++r)
+                if (srcs[r].first != r)  // collected in rank order: one per rank means srcs[r] is rank r
+                    return PL_ERR_LAYOUT;
+        }
+        for (auto [r, i] : srcs) {
+            const pl_part& p = in.parts[i];
+            if (region_count(p) != t.count)
+                return PL_ERR_LAYOUT;
+            t.srcs.push_back(Region{PL_SPACE_IN, r, p.offset, p.rows, p.len, p.row_stride});
+        }
+    }
+    return PL_OK;
+}
+
+// Gives every region of a transfer the same row structure: strided regions
+// keep theirs (they must agree on the row length), contiguous ones are cut
+// into rows of that length.
+pl_status normalise_rows(Transfer& t)
+{
+    uint64_t L = 0;
+    auto visit = [&](const Region& g) -> bool {
+        if (g.rows > 1) {
+            if (L == 0)
+                L = g.cols;
+            else if (g.cols != L)
+                return false;
+        }
+        return true;
+    };
+    for (auto& g : t.srcs)
+        if (!visit(g))
+            return PL_ERR_UNSUPPORTED;
+    for (auto& g : t.dsts)
+        if (!visit(g))
+            return PL_ERR_UNSUPPORTED;
+    auto fix = [&](Region& g) {
+        if (L == 0 || t.count == 0) {
+            g.rows = 1;
+            g.cols = t.count;
+            g.stride = t.count;
+        } else if (g.rows == 1) {
+            g.rows = t.count / L;
+            g.cols = L;
+            g.stride = L;
+        }
+    };
+    for (auto& g : t.srcs)
+        fix(g);
+    for (auto& g : t.dsts)
+        fix(g);
+    return PL_OK;
+}
+
+// Chunks of a transfer.  One-row transfers are cut at element boundaries that
+// keep the first destination 16-byte aligned after its first chunk; multi-row
+// transfers are cut into row ranges, or row pieces when a row exceeds a chunk.
+std::vector<Chunk> make_chunks(const Transfer& t, uint64_t chunk_elems, uint64_t vec_elems)
+{
+    std::vector<Chunk> out;
+    if (t.count == 0)
+        return out;
+    const Region& d0 = t.dsts[0];
+    auto cut_row = [&](uint64_t row, uint64_t cols, uint64_t dst_off) {
+        uint64_t head = (vec_elems - dst_off % vec_elems) % vec_elems;
+        uint64_t c0 = 0;
+        while (c0 < cols) {
+            uint64_t n = chunk_elems;
+            if (c0 == 0)
+                n += head;
+            n = std::min(n, cols - c0);
+            out.push_back(Chunk{row, 1, c0, n});
+            c0 += n;
+        }
+    };
+    if (d0.rows == 1) {
+        cut_row(0, d0.cols, d0.offset);
+    } else if (d0.cols >= chunk_elems) {
+        for (uint64_t r = 0; r < d0.rows; ++r)
+            cut_row(r, d0.cols, d0.offset + r * d0.stride);
+    } else {
+        uint64_t per = std::max<uint64_t>(1, chunk_elems / d0.cols);
+        for (uint64_t r = 0; r < d0.rows; r += per)
+            out.push_back(Chunk{r, std::min(per, d0.rows - r), 0, d0.cols});
+    }
+    return out;
+}
+
+class Builder {
+public:
+    Builder(HostPlan& hp, int R) : hp_(hp), R_(R) {}
+
+    Ref region(const Region& g, const Chunk& c) const
+    {
+        Ref f{};
+        f.buf = (uint32_t)(g.space == PL_SPACE_IN ? g.rank : R_ + g.rank);
+        f.offset = g.offset + c.row0 * g.stride + c.col0;
+        f.stride = g.stride;
+        return f;
+    }
+
+    Ref slot(uint64_t s, uint64_t slot_elems, const Chunk& c) const
+    {
+        Ref f{};
+        f.buf = (uint32_t)(2 * R_);
+        f.offset = s * slot_elems;
+        f.stride = c.ncols;
+        return f;
+    }
+
+    struct Pending {
+        std::vector<Ref> src, dst;
+        std::vector<Sync> waits, posts;
+    };
+
+    void emit(const Pending& p, ItemKind kind, pl_op op, const Chunk& c)
+    {
+        Item it{};
+        it.kind = kind;
+        it.op = (uint8_t)(op == PL_SUM && p.src.size() > 1 ? 1 : 0);
+        it.nsrc = (uint16_t)p.src.size();
+        it.ndst = (uint16_t)p.dst.size();
+        it.rows = (uint32_t)c.nrows;
+        it.cols = c.ncols;
+        it.ref = (uint32_t)hp_.refs.size();
+        hp_.refs.insert(hp_.refs.end(), p.src.begin(), p.src.end());
+        hp_.refs.insert(hp_.refs.end(), p.dst.begin(), p.dst.end());
+        it.sync = (uint32_t)hp_.syncs.size();
+        it.nwait = (uint16_t)p.waits.size();
+        it.npost = (uint16_t)p.posts.size();
+        hp_.syncs.insert(hp_.syncs.end(), p.waits.begin(), p.waits.end());
+        hp_.syncs.insert(hp_.syncs.end(), p.posts.begin(), p.posts.end());
+        hp_.items.push_back(it);
+    }
+
+private:
+    HostPlan& hp_;
+    int R_;
+};
+
+Sync mk_sync(SyncType t, uint32_t flag, uint32_t use, uint32_t count = 0)
+{
+    Sync s{};
+    s.type = t;
+    s.flag = flag;
+    s.use = use;
+    s.count = count;
+    return s;
+}
+
+// Checks that every wait of item j is satisfied by items with smaller
+// indices, so that CTAs claiming items in index order always progress.
+bool waits_precede(const HostPlan& hp)
+{
+    std::map<std::pair<uint32_t, uint32_t>, uint64_t> notified;            // (flag, use) -> item
+    std::map<std::pair<uint32_t, uint32_t>, std::pair<uint64_t, uint32_t>> credits;  // -> (last item, n)
+    std::map<std::pair<uint32_t, uint32_t>, uint32_t> credit_need;
+    for (uint64_t j = 0; j < hp.items.size(); ++j) {
+        const Item& it = hp.items[j];
+        for (uint32_t k = it.nwait; k < (uint32_t)it.nwait + it.npost; ++k) {
+            const Sync& s = hp.syncs[it.sync + k];
+            auto key = std::make_pair(s.flag, s.use);
+            if (s.type == kNotify)
+                notified[key] = j;
+            else if (s.type == kCredit) {
+                auto& c = credits[key];
+                c.first = j;
+                c.second += 1;
+                credit_need[key] = s.count;
+            }
+        }
+    }
+    for (uint64_t j = 0; j < hp.items.size(); ++j) {
+        const Item& it = hp.items[j];
+        for (uint32_t k = 0; k < it.nwait; ++k) {
+            const Sync& s = hp.syncs[it.sync + k];
+            auto key = std::make_pair(s.flag, s.use);
+            if (s.type == kWaitFull) {
+                auto f = notified.find(key);
+                if (f == notified.end() || f->second >= j)
+                    return false;
+            } else {
+                auto c = credits.find(key);
+                if (c == credits.end() || c->second.first >= j || c->second.second != credit_need[key])
+                    return false;
+            }
+        }
+    }
+    return true;
+}
+
+pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                 const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, HostPlan& hp)
+{
+    if (in.R != R || out.R != R)
+        return PL_ERR_INVALID;
+    hp = HostPlan{};
+    hp.R = R;
+    hp.dtype = dt;
+    const uint64_t S = elem_size(dt);
+    const uint64_t E = 16 / S;
+
+    std::vector<Transfer> ts;
+    pl_status st = collect_transfers(in, out, op, R, ts);
+    if (st != PL_OK)
+        return st;
+    uint64_t total_bytes = 0;
+    for (Transfer& t : ts) {
+        if ((st = normalise_rows(t)) != PL_OK)
+            return st;
+        total_bytes += t.count * S;
+    }
+
+    const int full_grid = std::max(1, num_sms) * std::max(1, ctas_per_sm);
+    uint64_t chunk_bytes = pol.chunk_bytes;
+    if (chunk_bytes == 0) {
+        chunk_bytes = total_bytes / ((uint64_t)full_grid * kItemsPerCta);
+        chunk_bytes = std::min(std::max(chunk_bytes, kMinChunkBytes), kMaxChunkBytes);
+    }
+    chunk_bytes = std::max<uint64_t>(256, chunk_bytes / 256 * 256);
+
+    const bool staged = pol.path == PL_PATH_STAGED;
+    if (staged && pol.chunk_bytes == 0) {
+        uint64_t per_rank = scratch_bytes / (uint64_t)R;
+        chunk_bytes = std::min(chunk_bytes, std::max<uint64_t>(256, per_rank / 4 / 256 * 256));
+    }
+    const uint64_t chunk_elems = std::max<uint64_t>(E, chunk_bytes / S / E * E);
+    // A slot holds one chunk; the first chunk of a row may carry up to one
+    // vector more (the head that aligns the destination).
+    const uint64_t slot_elems = chunk_elems + E;
+    uint64_t slots_per_rank = 0;
+    if (staged) {
+        // The ring of each rank holds at least 2 slots (a reducer re-stages
+        // its result into its own ring while its inputs are still held).
+        uint64_t per_rank = scratch_bytes / (uint64_t)R;
+        slots_per_rank = per_rank / (slot_elems * S);
+        if (slots_per_rank < 2)
+            return PL_ERR_NOMEM;
+    }
+
+    std::vector<std::vector<Chunk>> chunks(ts.size());
+    size_t max_chunks = 0;
+    for (size_t i = 0; i < ts.size(); ++i) {
+        chunks[i] = make_chunks(ts[i], chunk_elems, E);
+        max_chunks = std::max(max_chunks, chunks[i].size());
+    }
+
+    Builder b(hp, R);
+    bool tickets = false;
+    uint32_t next_flag = 0;
+    // staged ring bookkeeping
+    std::vector<uint64_t> cursor(R, 0);
+    std::vector<uint32_t> uses;
+    if (staged)
+        uses.assign((size_t)R * slots_per_rank, 0);
+    uint64_t bytes_read = 0, bytes_written = 0;
+
+    auto owner_of = [&](const Transfer& t) -> size_t {
+        for (size_t d = 0; d < t.dsts.size(); ++d)
+            if ((uint64_t)t.dsts[d].rank == t.name)
+                return d;
+        return 0;
+    };
+
+    auto stage = [&](int rank, uint32_t& slot_out, uint32_t& use_out) -> pl_status {
+        uint64_t s = (uint64_t)rank * slots_per_rank + (cursor[rank]++ % slots_per_rank);
+        if (uses[s] >= kMaxUsesPerLaunch)
+            return PL_ERR_UNSUPPORTED;
+        slot_out = (uint32_t)s;
+        use_out = uses[s]++;
+        return PL_OK;
+    };
+
+    for (size_t c = 0; c < max_chunks; ++c) {
+        for (size_t ti = 0; ti < ts.size(); ++ti) {
+            if (c >= chunks[ti].size())
+                continue;
+            const Transfer& t = ts[ti];
+            const Chunk& ch = chunks[ti][c];
+            const uint64_t blk = ch.nrows * ch.ncols * S;
+            const bool sum = op == PL_SUM && t.srcs.size() > 1;
+
+            if (!staged) {
+                if (sum && t.dsts.size() > 1 && pol.ar_form == PL_AR_COMPOSED) {
+                    // Figure 6, zero-staging: the owner reduces the chunk into its
+                    // output and notifies; every other rank then copies it.
+                    tickets = true;
+                    size_t o = owner_of(t);
+                    uint32_t flag = next_flag++;
+                    Builder::Pending red;
+                    for (auto& g : t.srcs)
+                        red.src.push_back(b.region(g, ch));
+                    red.dst.push_back(b.region(t.dsts[o], ch));
+                    red.posts.push_back(mk_sync(kNotify, flag, 0));
+                    b.emit(red, kMove, op, ch);
+                    bytes_read += blk * t.srcs.size();
+                    bytes_written += blk;
+                    for (size_t d = 0; d < t.dsts.size(); ++d) {
+                        if (d == o)
+                            continue;
+                        Builder::Pending ag;
+                        ag.src.push_back(b.region(t.dsts[o], ch));
+                        ag.dst.push_back(b.region(t.dsts[d], ch));
+                        ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
+                        b.emit(ag, kConsume, PL_COPY, ch);
+                        bytes_read += blk;
+                        bytes_written += blk;
+                    }
+                } else {
+                    // Zero-staging Consume: read the sources, write every destination.
+                    for (size_t d0 = 0; d0 < t.dsts.size(); d0 += kMaxRanks) {
+                        Builder::Pending mv;
+                        for (auto& g : t.srcs)
+                            mv.src.push_back(b.region(g, ch));
+                        size_t d1 = std::min(t.dsts.size(), d0 + kMaxRanks);
+                        for (size_t d = d0; d < d1; ++d)
+                            mv.dst.push_back(b.region(t.dsts[d], ch));
+                        b.emit(mv, kMove, op, ch);
+                        bytes_read += blk * t.srcs.size();
+                        bytes_written += blk * (d1 - d0);
+                    }
+                }
+                continue;
+            }
+
+            // Staged SNAC: every source rank stages its chunk into its ring and
+            // notifies; consumers wait, copy or reduce from the ring, and credit
+            // the slot so its producer may reuse it.
+            tickets = true;
+            std::vector<uint32_t> slot(t.srcs.size()), use(t.srcs.size());
+            for (size_t s = 0; s < t.srcs.size(); ++s) {
+                if ((st = stage(t.srcs[s].rank, slot[s], use[s])) != PL_OK)
+                    return st;
+                Builder::Pending sg;
+                sg.src.push_back(b.region(t.srcs[s], ch));
+                sg.dst.push_back(b.slot(slot[s], slot_elems, ch));
+                if (use[s] > 0)
+                    sg.waits.push_back(mk_sync(kWaitFree, slot[s], use[s] - 1));
+                sg.posts.push_back(mk_sync(kNotify, slot[s], use[s]));
+                b.emit(sg, kStage, PL_COPY, ch);
+                bytes_read += blk;
+                bytes_written += blk;
+            }
+            if (!sum) {
+                // COPY: one consumer per destination rank, each reading the slot.
+                uint32_t n = (uint32_t)t.dsts.size();
+                for (size_t d = 0; d < t.dsts.size(); ++d) {
+                    Builder::Pending cs;
+                    cs.src.push_back(b.slot(slot[0], slot_elems, ch));
+                    cs.dst.push_back(b.region(t.dsts[d], ch));
+                    cs.waits.push_back(mk_sync(kWaitFull, slot[0], use[0]));
+                    cs.posts.push_back(mk_sync(kCredit, slot[0], use[0], n));
+                    b.emit(cs, kConsume, PL_COPY, ch);
+                    bytes_read += blk;
+                    bytes_written += blk;
+                }
+            } else if (t.dsts.size() == 1 || pol.ar_form == PL_AR_FUSED) {
+                // SUM: one consumer reduces the R staged chunks into every destination.
+                Builder::Pending cs;
+                for (size_t s = 0; s < t.srcs.size(); ++s)
+                    cs.src.push_back(b.slot(slot[s], slot_elems, ch));
+                for (auto& g : t.dsts)
+                    cs.dst.push_back(b.region(g, ch));
+                for (size_t s = 0; s < t.srcs.size(); ++s) {
+                    cs.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
+                    cs.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
+                }
+                b.emit(cs, kConsume, op, ch);
+                bytes_read += blk * t.srcs.size();
+                bytes_written += blk * t.dsts.size();
+            } else {
+                // Figure 6: the owner reduces, writes its output and re-stages the
+                // reduced chunk into its own ring; the other ranks gather it.
+                size_t o = owner_of(t);
+                uint32_t yslot, yuse;
+                if ((st = stage(t.dsts[o].rank, yslot, yuse)) != PL_OK)
+                    return st;
+                Builder::Pending red;
+                for (size_t s = 0; s < t.srcs.size(); ++s)
+                    red.src.push_back(b.slot(slot[s], slot_elems, ch));
+                red.dst.push_back(b.region(t.dsts[o], ch));
+                red.dst.push_back(b.slot(yslot, slot_elems, ch));
+                for (size_t s = 0; s < t.srcs.size(); ++s)
+                    red.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
+                if (yuse > 0)
+                    red.waits.push_back(mk_sync(kWaitFree, yslot, yuse - 1));
+                for (size_t s = 0; s < t.srcs.size(); ++s)
+                    red.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
+                red.posts.push_back(mk_sync(kNotify, yslot, yuse));
+                b.emit(red, kConsume, op, ch);
+                bytes_read += blk * t.srcs.size();
+                bytes_written += 2 * blk;
+                uint32_t n = (uint32_t)t.dsts.size() - 1;
+                for (size_t d = 0; d < t.dsts.size(); ++d) {
+                    if (d == o)
+                        continue;
+                    Builder::Pending ag;
+                    ag.src.push_back(b.slot(yslot, slot_elems, ch));
+                    ag.dst.push_back(b.region(t.dsts[d], ch));
+                    ag.waits.push_back(mk_sync(kWaitFull, yslot, yuse));
+                    ag.posts.push_back(mk_sync(kCredit, yslot, yuse, n));
+                    b.emit(ag, kConsume, PL_COPY, ch);
+                    bytes_read += blk;
+                    bytes_written += blk;
+                }
+            }
+        }
+    }
+
+    if (hp.items.size() >= (1ull << 31) || hp.refs.size() >= (1ull << 32) || hp.syncs.size() >= (1ull << 32))
+        return PL_ERR_UNSUPPORTED;
+    hp.nflags = staged ? (uint32_t)((uint64_t)R * slots_per_rank) : next_flag;
+    for (const Item& it : hp.items) {
+        if (it.nsrc > kMaxRanks || it.ndst > kMaxRanks || it.nsrc == 0 || it.ndst == 0)
+            return PL_ERR_UNSUPPORTED;  // the kernel holds at most 64 sources and 64 destinations
+        hp.ops |= it.op ? kOpsSum : kOpsCopy;
+    }
+    if (tickets && !waits_precede(hp))
+        return PL_ERR_NOMEM;
+
+    int ctas = pol.ctas ? pol.ctas : full_grid;
+    if (!tickets)
+        ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
+    else
+        ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
+    ctas = std::max(1, ctas);
+
+    pl_plan_stats& s = hp.stats;
+    s.items = hp.items.size();
+    s.refs = hp.refs.size();
+    s.syncs = hp.syncs.size();
+    s.flags = hp.nflags;
+    s.chunk_elems = chunk_elems;
+    s.slots = slots_per_rank;
+    s.slot_elems = staged ? slot_elems : 0;
+    s.ctas = ctas;
+    s.threads = kThreads;
+    s.uses_tickets = tickets ? 1 : 0;
+    s.path = pol.path;
+    s.bytes_read = bytes_read;
+    s.bytes_written = bytes_written;
+    return PL_OK;
+}
+
+}  // namespace
+
+// -------------------------------------------------------- plan introspection
+
+struct pl_plan {
+    HostPlan hp;
+};
+
+extern "C" {
+
+PL_API pl_status pl_plan_create(pl_plan** plan, const pl_layout* in, const pl_layout* out, pl_op op,
+                                pl_dtype dtype, int R, const pl_policy* policy, int num_sms,
+                                uint64_t scratch_bytes)
+{
+    if (!plan || !in || !out || R < 1 || R > kMaxRanks || num_sms < 1)
+        return PL_ERR_INVALID;
+    if ((op != PL_COPY && op != PL_SUM) || (dtype != PL_BF16 && dtype != PL_FP32))
+        return PL_ERR_INVALID;
+    ResolvedPolicy rp;
+    pl_status st = resolve_policy(policy, rp);
+    if (st != PL_OK)
+        return st;
+    std::unique_ptr<pl_plan> p(new (std::nothrow) pl_plan);
+    if (!p)
+        return PL_ERR_NOMEM;
+    st = derive(*in, *out, op, dtype, R, rp, num_sms, kDefaultCtasPerSm, scratch_bytes, p->hp);
+    if (st != PL_OK)
+        return st;
+    *plan = p.release();
+    return PL_OK;
+}
+
+PL_API pl_status pl_plan_destroy(pl_plan* plan)
+{
+    delete plan;
+    return PL_OK;
+}
+
+PL_API pl_status pl_plan_get_stats(const pl_plan* plan, pl_plan_stats* stats)
+{
+    if (!plan || !stats)
+        return PL_ERR_INVALID;
+    *stats = plan->hp.stats;
+    return PL_OK;
+}
+
+PL_API pl_status pl_plan_get_item(const pl_plan* plan, uint64_t i, pl_plan_item* item, pl_plan_ref* refs,
+                                  int max_refs, pl_plan_sync* syncs, int max_syncs)
+{
+    if (!plan || !item || i >= plan->hp.items.size())
+        return PL_ERR_INVALID;
+    const HostPlan& hp = plan->hp;
+    const Item& it = hp.items[i];
+    item->kind = it.kind;
+    item->op = it.op;
+    item->nsrc = it.nsrc;
+    item->ndst = it.ndst;
+    item->nwait = it.nwait;
+    item->npost = it.npost;
+    item->rows = it.rows;
+    item->cols = it.cols;
+    int nref = it.nsrc + it.ndst;
+    if (refs) {
+        if (max_refs < nref)
+            return PL_ERR_INVALID;
+        for (int k = 0; k < nref; ++k) {
+            const Ref& f = hp.refs[it.ref + k];
+            int R = hp.R;
+            pl_plan_ref& o = refs[k];
+            if ((int)f.buf < R) {
+                o.space = PL_SPACE_IN;
+                o.index = (int)f.buf;
+            } else if ((int)f.buf < 2 * R) {
+                o.space = PL_SPACE_OUT;
+                o.index = (int)f.buf - R;
+            } else {
+                o.space = PL_SPACE_SCRATCH;
+                o.index = 0;
+            }
+            o.offset = f.offset;
+            o.stride = f.stride;
+        }
+    }
+    int nsync = it.nwait + it.npost;
+    if (syncs) {
+        if (max_syncs < nsync)
+            return PL_ERR_INVALID;
+        for (int k = 0; k < nsync; ++k) {
+            const Sync& s = hp.syncs[it.sync + k];
+            syncs[k].type = s.type;
+            syncs[k].flag = s.flag;
+            syncs[k].use = s.use;
+            syncs[k].count = s.count;
+        }
+    }
+    return PL_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ context
+
+namespace {
+
+struct DevicePlan {
+    HostPlan hp;  // host copy (stats, counts)
+    void* mem = nullptr;
+    const Item* items = nullptr;
+    const Ref* refs = nullptr;
+    const Sync* syncs = nullptr;
+};
+
+class DeviceGuard {
+public:
+    explicit DeviceGuard(int dev)
+    {
+        ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+        if (ok_ && prev_ != dev)
+            ok_ = cudaSetDevice(dev) == cudaSuccess;
+        dev_ = dev;
+    }
+    ~DeviceGuard()
+    {
+        if (prev_ != dev_)
+            cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+private:
+    int prev_ = -1, dev_ = -1;
+    bool ok_ = false;
+};
+
+}  // namespace
+
+struct pl_ctx {
+    int device = 0;
+    int num_sms = 0;
+    int ctas_per_sm = kDefaultCtasPerSm;
+    void* state_mem = nullptr;
+    DeviceState st{};
+    uint32_t flag_capacity = 0;
+    char* scratch = nullptr;
+    uint64_t scratch_bytes = 0;
+    unsigned long long epoch = 0;
+    uint64_t launches = 0;
+    int last_cuda_error = 0;
+    std::unordered_map<std::string, std::unique_ptr<DevicePlan>> cache;
+    std::map<std::pair<int, uint64_t>, pl_layout*> ar_layouts;
+};
+
+namespace {
+
+pl_status cuda_fail(pl_ctx* ctx, cudaError_t e)
+{
+    ctx->last_cuda_error = (int)e;
+    cudaGetLastError();  // clear a sticky-free error so later calls see their own
+    return e == cudaErrorMemoryAllocation ? PL_ERR_NOMEM : PL_ERR_CUDA;
+}
+
+// (Re)allocates the flag arrays so that at least n flags exist; all zero.
+pl_status ensure_flags(pl_ctx* ctx, uint32_t n)
+{
+    if (n <= ctx->flag_capacity && ctx->state_mem)
+        return PL_OK;
+    uint32_t cap = std::max<uint32_t>(std::max<uint32_t>(n, 4096), ctx->flag_capacity * 2);
+    size_t bytes = (size_t)cap * (8 + 8 + 4) + 64;
+    void* mem = nullptr;
+    if (ctx->state_mem) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(ctx, e);
+    }
+    cudaError_t e = cudaMalloc(&mem, bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    e = cudaMemset(mem, 0, bytes);
+    if (e != cudaSuccess) {
+        cudaFree(mem);
+        return cuda_fail(ctx, e);
+    }
+    if (ctx->state_mem)
+        cudaFree(ctx->state_mem);
+    ctx->state_mem = mem;
+    ctx->flag_capacity = cap;
+    char* p = (char*)mem;
+    ctx->st.full = (unsigned long long*)p;
+    ctx->st.done = (unsigned long long*)(p + (size_t)cap * 8);
+    ctx->st.count = (unsigned int*)(p + (size_t)cap * 16);
+    char* tail = p + (size_t)cap * 20;
+    tail = (char*)(((uintptr_t)tail + 15) & ~(uintptr_t)15);
+    ctx->st.ticket = (unsigned int*)tail;
+    ctx->st.exited = (unsigned int*)(tail + 4);
+    ctx->st.status = (int*)(tail + 8);
+    ctx->st.abort = (int*)(tail + 12);
+    return PL_OK;
+}
+
+std::string plan_key(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                     const ResolvedPolicy& rp)
+{
+    std::string k;
+    auto put = [&](const void* p, size_t n) { k.append((const char*)p, n); };
+    put(&op, sizeof op);
+    put(&dt, sizeof dt);
+    put(&R, sizeof R);
+    put(&rp.path, sizeof rp.path);
+    put(&rp.ar_form, sizeof rp.ar_form);
+    put(&rp.ctas, sizeof rp.ctas);
+    put(&rp.chunk_bytes, sizeof rp.chunk_bytes);
+    for (const pl_layout* L : {&in, &out}) {
+        put(L->first.data(), L->first.size() * sizeof(int));
+        put(L->parts.data(), L->parts.size() * sizeof(pl_part));
+    }
+    return k;
+}
+
+pl_status get_plan(pl_ctx* ctx, const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                   const ResolvedPolicy& rp, DevicePlan*& dp)
+{
+    std::string key = plan_key(in, out, op, dt, R, rp);
+    auto it = ctx->cache.find(key);
+    if (it != ctx->cache.end()) {
+        dp = it->second.get();
+        return PL_OK;
+    }
+    std::unique_ptr<DevicePlan> p(new (std::nothrow) DevicePlan);
+    if (!p)
+        return PL_ERR_NOMEM;
+    pl_status st = derive(in, out, op, dt, R, rp, ctx->num_sms, ctx->ctas_per_sm, ctx->scratch_bytes, p->hp);
+    if (st != PL_OK)
+        return st;
+    size_t bi = p->hp.items.size() * sizeof(Item);
+    size_t br = p->hp.refs.size() * sizeof(Ref);
+    size_t bs = p->hp.syncs.size() * sizeof(Sync);
+    size_t oi = 0, orr = (bi + 255) / 256 * 256, os = orr + (br + 255) / 256 * 256;
+    size_t total = std::max<size_t>(256, os + bs);
+    if (ctx->cache.size() >= kMaxCachedPlans) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(ctx, e);
+        for (auto& kv : ctx->cache)
+            cudaFree(kv.second->mem);
+        ctx->cache.clear();
+    }
+    cudaError_t e = cudaMalloc(&p->mem, total);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    std::vector<char> host(total, 0);
+    if (bi)
+        std::memcpy(host.data() + oi, p->hp.items.data(), bi);
+    if (br)
+        std::memcpy(host.data() + orr, p->hp.refs.data(), br);
+    if (bs)
+        std::memcpy(host.data() + os, p->hp.syncs.data(), bs);
+    e = cudaMemcpy(p->mem, host.data(), total, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(p->mem);
+        return cuda_fail(ctx, e);
+    }
+    p->items = (const Item*)((char*)p->mem + oi);
+    p->refs = (const Ref*)((char*)p->mem + orr);
+    p->syncs = (const Sync*)((char*)p->mem + os);
+    // The device copy holds everything the kernel needs; keep host vectors only
+    // for stats.
+    p->hp.items.clear();
+    p->hp.items.shrink_to_fit();
+    p->hp.refs.clear();
+    p->hp.refs.shrink_to_fit();
+    p->hp.syncs.clear();
+    p->hp.syncs.shrink_to_fit();
+    dp = p.get();
+    ctx->cache.emplace(std::move(key), std::move(p));
+    return PL_OK;
+}
+
+struct Interval {
+    uintptr_t lo, hi;
+    bool is_out;
+    int rank;
+    const pl_part* part;
+};
+
+// Checks every part against its buffer, element alignment, and the alias
+// rule: an output may only coincide exactly with one of its own sources.
+pl_status check_buffers(const pl_layout& in, const pl_layout& out, pl_dtype dt, int R,
+                        void* const* in_bufs, const uint64_t* in_counts,
+                        void* const* out_bufs, const uint64_t* out_counts)
+{
+    const uint64_t S = elem_size(dt);
+    std::vector<Interval> iv;
+    for (int side = 0; side < 2; ++side) {
+        const pl_layout& L = side ? out : in;
+        void* const* bufs = side ? out_bufs : in_bufs;
+        const uint64_t* counts = side ? out_counts : in_counts;
+        for (int r = 0; r < R; ++r) {
+            if (counts[r] > 0 && !bufs[r])
+                return PL_ERR_INVALID;
+            if (bufs[r] && ((uintptr_t)bufs[r] % S))
+                return PL_ERR_INVALID;
+            for (int i = L.first[r]; i < L.first[r + 1]; ++i) {
+                const pl_part& p = L.parts[i];
+                if (region_count(p) == 0)
+                    continue;
+                if (region_extent(p) > counts[r])
+                    return PL_ERR_LAYOUT;
+                uintptr_t lo = (uintptr_t)bufs[r] + p.offset * S;
+                uintptr_t hi = (uintptr_t)bufs[r] + region_extent(p) * S;
+                iv.push_back(Interval{lo, hi, side == 1, r, &p});
+            }
+        }
+    }
+    std::sort(iv.begin(), iv.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
+    for (size_t i = 0; i < iv.size(); ++i) {
+        for (size_t j = i + 1; j < iv.size() && iv[j].lo < iv[i].hi; ++j) {
+            const Interval& a = iv[i];
+            const Interval& b = iv[j];
+            if (!a.is_out && !b.is_out)
+                continue;  // inputs may overlap each other
+            if (a.is_out && b.is_out)
+                return PL_ERR_ALIAS;
+            const Interval& o = a.is_out ? a : b;
+            const Interval& n = a.is_out ? b : a;
+            bool exact = o.lo == n.lo && o.hi == n.hi && o.part->name == n.part->name &&
+                         o.part->rows == n.part->rows && o.part->len == n.part->len &&
+                         (o.part->rows == 1 || o.part->row_stride == n.part->row_stride);
+            if (!exact)
+                return PL_ERR_ALIAS;
+        }
+    }
+    return PL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PL_API pl_status pl_ctx_create(pl_ctx** out, int device, uint64_t scratch_bytes)
+{
+    if (!out || device < 0)
+        return PL_ERR_INVALID;
+    *out = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+        cudaGetLastError();
+        return PL_ERR_CUDA;
+    }
+    std::unique_ptr<pl_ctx> ctx(new (std::nothrow) pl_ctx);
+    if (!ctx)
+        return PL_ERR_NOMEM;
+    ctx->device = device;
+    DeviceGuard g(device);
+    if (!g.ok())
+        return cuda_fail(ctx.get(), cudaGetLastError());
+    cudaError_t e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx.get(), e);
+    int occ = snac_ctas_per_sm(false, 0);
+    if (occ > 0)
+        ctx->ctas_per_sm = std::min(occ, kDefaultCtasPerSm);
+    pl_status st = ensure_flags(ctx.get(), 4096);
+    if (st != PL_OK)
+        return st;
+    if (scratch_bytes) {
+        e = cudaMalloc((void**)&ctx->scratch, scratch_bytes);
+        if (e != cudaSuccess) {
+            cudaFree(ctx->state_mem);
+            return cuda_fail(ctx.get(), e);
+        }
+        ctx->scratch_bytes = scratch_bytes;
+    }
+    *out = ctx.release();
+    return PL_OK;
+}
+
+PL_API pl_status pl_ctx_destroy(pl_ctx* ctx)
+{
+    if (!ctx)
+        return PL_OK;
+    {
+        DeviceGuard g(ctx->device);
+        cudaDeviceSynchronize();
+        for (auto& kv : ctx->cache)
+            cudaFree(kv.second->mem);
+        if (ctx->state_mem)
+            cudaFree(ctx->state_mem);
+        if (ctx->scratch)
+            cudaFree(ctx->scratch);
+        for (auto& kv : ctx->ar_layouts)
+            delete kv.second;
+    }
+    delete ctx;
+    return PL_OK;
+}
+
+PL_API int pl_ctx_cuda_error(const pl_ctx* ctx) { return ctx ? ctx->last_cuda_error : 0; }
+
+PL_API uint64_t pl_ctx_launches(const pl_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+PL_API pl_status pl_ctx_status(pl_ctx* ctx, void* stream)
+{
+    if (!ctx)
+        return PL_ERR_INVALID;
+    DeviceGuard g(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    int host[2] = {0, 0};
+    e = cudaMemcpy(host, ctx->st.status, sizeof host, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    if (host[0] == 0)
+        return PL_OK;
+    // A wait gave up: flags may be half-updated.  Start the next launch clean.
+    size_t bytes = (size_t)ctx->flag_capacity * 20 + 64;
+    e = cudaMemset(ctx->state_mem, 0, bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    return host[0];
+}
+
+PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout* out, pl_op op, pl_dtype dt,
+                               int R, void* const* in_bufs, const uint64_t* in_counts, void* const* out_bufs,
+                               const uint64_t* out_counts, const pl_policy* policy, void* stream)
+{
+    if (!ctx || !in || !out || !in_bufs || !out_bufs || !in_counts || !out_counts)
+        return PL_ERR_INVALID;
+    if (R < 1 || R > kMaxRanks || in->R != R || out->R != R)
+        return PL_ERR_INVALID;
+    if ((op != PL_COPY && op != PL_SUM) || (dt != PL_BF16 && dt != PL_FP32))
+        return PL_ERR_INVALID;
+    ResolvedPolicy rp;
+    pl_status st = resolve_policy(policy, rp);
+    if (st != PL_OK)
+        return st;
+    if ((st = check_buffers(*in, *out, dt, R, in_bufs, in_counts, out_bufs, out_counts)) != PL_OK)
+        return st;
+    DeviceGuard g(ctx->device);
+    if (!g.ok())
+        return cuda_fail(ctx, cudaGetLastError());
+    DevicePlan* dp = nullptr;
+    if ((st = get_plan(ctx, *in, *out, op, dt, R, rp, dp)) != PL_OK)
+        return st;
+    const pl_plan_stats& ps = dp->hp.stats;
+    if (ps.items == 0)
+        return PL_OK;  // nothing to move
+    if ((st = ensure_flags(ctx, dp->hp.nflags)) != PL_OK)
+        return st;
+    LaunchArgs a{};
+    a.items = dp->items;
+    a.refs = dp->refs;
+    a.syncs = dp->syncs;
+    a.nitems = (uint32_t)ps.items;
+    a.use_tickets = ps.uses_tickets;
+    a.dtype = dt;
+    a.nbufs = 2 * R + 1;
+    a.ops = dp->hp.ops;
+    a.epoch = ++ctx->epoch;
+    a.timeout_ns = rp.timeout_ns;
+    a.drop_notify = rp.drop_notify;
+    a.st = ctx->st;
+    for (int r = 0; r < R; ++r) {
+        a.bufs[r] = (char*)in_bufs[r];
+        a.bufs[R + r] = (char*)out_bufs[r];
+    }
+    a.bufs[2 * R] = ctx->scratch;
+    bool bulk = rp.datapath == PL_ATOM_BULK;
+    cudaError_t e = launch_snac(a, ps.ctas, bulk, rp.stages, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e);
+    ++ctx->launches;
+    return PL_OK;
+}
+
+PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dt, int R, uint64_t count, void* const* in_bufs,
+                              void* const* out_bufs, const pl_policy* policy, void* stream)
+{
+    if (!ctx || R < 1 || R > kMaxRanks)
+        return PL_ERR_INVALID;
+    auto key = std::make_pair(R, count);
+    auto it = ctx->ar_layouts.find(key);
+    if (it == ctx->ar_layouts.end()) {
+        std::vector<uint64_t> lens(R, count / (uint64_t)R);
+        lens[R - 1] = count - (count / (uint64_t)R) * (uint64_t)(R - 1);
+        pl_layout* L = nullptr;
+        pl_status st = pl_layout_partitioned(&L, R, lens.data());
+        if (st != PL_OK)
+            return st;
+        it = ctx->ar_layouts.emplace(key, L).first;
+    }
+    std::vector<uint64_t> counts(R, count);
+    return pl_collective(ctx, it->second, it->second, PL_SUM, dt, R, in_bufs, counts.data(), out_bufs,
+                         counts.data(), policy, stream);
+}
+
+}  // extern "C"

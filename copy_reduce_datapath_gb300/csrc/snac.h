@@ -1,0 +1,99 @@
+// Internal layout of a SNAC work list as the device reads it, and the launch
+// interface between the host runtime (runtime.cpp) and the Atom kernels
+// (atom.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace purlin {
+
+constexpr int kMaxRanks = 64;
+constexpr int kMaxRefsPerItem = 2 * kMaxRanks + 1;  // R sources + R destinations + one slot
+constexpr int kThreads = 512;                        // threads per CTA of the persistent grid
+constexpr int kBulkMaxStages = 8;
+
+enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2 };
+enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3 };
+
+// Which moves a work list contains: the kernel is instantiated per mix so that
+// a copy-only or sum-only list gets code without the other path.
+constexpr int kOpsCopy = 1;
+constexpr int kOpsSum = 2;
+
+// One work item: move a rows x cols block from nsrc sources (copy if nsrc == 1,
+// rank-ordered fp32 sum otherwise) into ndst destinations.  Refs
+// [ref, ref + nsrc) are sources, [ref + nsrc, ref + nsrc + ndst) destinations.
+// Syncs [sync, sync + nwait) run before the move, [sync + nwait, + npost) after.
+struct Item {
+    uint8_t kind;
+    uint8_t op;        // 0 copy, 1 sum
+    uint16_t nsrc;
+    uint16_t ndst;
+    uint16_t nwait;
+    uint32_t ref;
+    uint32_t sync;
+    uint32_t rows;
+    uint16_t npost;
+    uint16_t pad;
+    uint64_t cols;
+};
+static_assert(sizeof(Item) == 32, "Item is 32 bytes");
+
+// A region reference: buffer slot `buf` of the launch's pointer table
+// (inputs 0..R-1, outputs R..2R-1, scratch 2R), element offset of row 0 and
+// element distance between rows.
+struct Ref {
+    uint32_t buf;
+    uint32_t pad;
+    uint64_t offset;
+    uint64_t stride;
+};
+static_assert(sizeof(Ref) == 24, "Ref is 24 bytes");
+
+struct Sync {
+    uint8_t type;
+    uint8_t pad[3];
+    uint32_t flag;
+    uint32_t use;
+    uint32_t count;
+};
+static_assert(sizeof(Sync) == 16, "Sync is 16 bytes");
+
+// Device-side SNAC state owned by a context.
+struct DeviceState {
+    unsigned long long* full;   // [nflags] notify tags
+    unsigned long long* done;   // [nflags] slot-free tags
+    unsigned int* count;        // [nflags] consumers seen for the current use
+    unsigned int* ticket;       // next item to claim
+    unsigned int* exited;       // CTAs that finished (the last one resets ticket/exited)
+    int* status;                // 0 ok, else a pl_status
+    int* abort;                 // set with status: every wait gives up at once
+};
+
+struct LaunchArgs {
+    const Item* items;
+    const Ref* refs;
+    const Sync* syncs;
+    uint32_t nitems;
+    int32_t use_tickets;
+    int32_t dtype;               // 0 bf16, 1 fp32
+    int32_t nbufs;
+    int32_t ops;                 // kOpsCopy | kOpsSum present in the list
+    int32_t pad0;
+    unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
+    unsigned long long timeout_ns;
+    long long drop_notify;       // item index whose notifies are skipped, or -1
+    DeviceState st;
+    char* bufs[kMaxRefsPerItem]; // inputs, outputs, scratch
+};
+
+// Launch of the persistent SNAC kernel (atom.cu).  `bulk` selects the
+// cp.async.bulk shared-memory ring for copy items with `stages` stages.
+cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream);
+
+// CTAs of the SNAC kernel that fit on one SM at once.
+int snac_ctas_per_sm(bool bulk, int stages);
+
+}  // namespace purlin

@@ -21,6 +21,8 @@ Generators
   (library rounding; used only to prepare inputs).
 * ``zipf_lengths``         -- partition lengths proportional to (i+1)^-s,
   largest-remainder rounding, then a seeded Fisher-Yates shuffle.
+* ``host_normal_bf16_torch`` -- N(0,1) bf16 from PyTorch's seeded CPU generator,
+  for large host-side samples.
 * ``device_normal_bf16`` / ``device_uniform_pm1`` -- large inputs drawn on the
   GPU by PyTorch's seeded Philox generator (too large to draw on the host in
   reasonable time); used for the full-size benchmark and sampled parity checks,
@@ -153,6 +155,15 @@ def equal_lengths(total: int, R: int) -> list[int]:
     """Equal split: the first R-1 partitions get total // R, the last gets the rest."""
     q = total // R
     return [q] * (R - 1) + [total - q * (R - 1)]
+
+
+def host_normal_bf16_torch(seed: int, rank: int, n: int):
+    """N(0,1) bf16 on the host from PyTorch's seeded CPU generator (fast; for large
+    host-side samples where the SplitMix64 Box-Muller stream would take minutes)."""
+    import torch
+    g = torch.Generator()
+    g.manual_seed(device_seed(seed, rank))
+    return torch.randn(n, generator=g, dtype=torch.float32).to(torch.bfloat16)
 
 
 def device_seed(seed: int, rank: int) -> int:

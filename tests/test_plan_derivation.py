@@ -1,0 +1,214 @@
+"""SNAC derivation on the host (no GPU): work lists derived from layout pairs,
+executed by a host emulation under random interleavings, equal the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from copy_reduce_datapath_gb300 import purlin as P
+
+import plan_interp
+
+NP = {"bf16": np.uint16, "fp32": np.float32}
+
+
+def rand(dtype, seed, rank, n):
+    t = synth.host_tensor("normal", dtype, seed, rank, n)
+    if dtype == "bf16":
+        import torch
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def policy(path, ar_form=P.PL_AR_AUTO, chunk=256):
+    return P.pl_policy_default(path=path, allreduce_form=ar_form, chunk_bytes=chunk)
+
+
+def plan_for(lin, lout, op, dtype, R, pol, scratch=0):
+    return P.pl_plan_create(lin, lout, op, dtype, R, pol, num_sms=4, scratch_bytes=scratch)
+
+
+PATHS = [(P.PL_PATH_ZS, 0), (P.PL_PATH_STAGED, 8 * 2 * 1024)]
+WINDOWS = [1, 3, 16]
+
+
+def run_and_check(plan, R, dtype, ins, outs, want, window, seed=0):
+    outs = [o.copy() for o in outs]
+    plan_interp.run(plan, R, dtype, ins, outs, window=window, seed=seed)
+    for r in range(R):
+        assert np.array_equal(outs[r], want[r]), f"rank {r}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("path,scratch", PATHS)
+@pytest.mark.parametrize("window", WINDOWS)
+def test_allgather_v(dtype, path, scratch, window):
+    R = 5
+    lens = [37, 0, 300, 1, 129]
+    ins = [rand(dtype, 1, r, lens[r]) for r in range(R)]
+    want = oracle.allgather(ins, dtype)
+    lin, lout = P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens)
+    pl = plan_for(lin, lout, "copy", dtype, R, policy(path), scratch)
+    outs = [np.zeros(sum(lens), NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("path,scratch", PATHS)
+@pytest.mark.parametrize("window", WINDOWS)
+def test_reducescatter_v(dtype, path, scratch, window):
+    R = 4
+    lens = [100, 3, 0, 250]
+    N = sum(lens)
+    ins = [rand(dtype, 2, r, N) for r in range(R)]
+    want = oracle.reducescatter(ins, lens, dtype)
+    lin, lout = P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens)
+    pl = plan_for(lin, lout, "sum", dtype, R, policy(path), scratch)
+    outs = [np.zeros(lens[k], NP[dtype]) for k in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
+
+
+@pytest.mark.parametrize("path,scratch", PATHS)
+def test_reducescatter_in_place(path, scratch):
+    R, dtype = 4, "bf16"
+    lens = [64, 65, 7, 200]
+    N = sum(lens)
+    ins = [rand(dtype, 3, r, N) for r in range(R)]
+    want = oracle.reducescatter(ins, lens, dtype)
+    lin, lout = P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned_inplace(R, lens)
+    pl = plan_for(lin, lout, "sum", dtype, R, policy(path), scratch)
+    bufs = [a.copy() for a in ins]
+    plan_interp.run(pl, R, dtype, bufs, bufs, window=8, seed=1)
+    o = 0
+    for k in range(R):
+        assert np.array_equal(bufs[k][o:o + lens[k]], want[k])
+        o += lens[k]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("path,scratch", PATHS)
+@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
+@pytest.mark.parametrize("window", WINDOWS)
+def test_allreduce(dtype, path, scratch, form, window):
+    R = 3
+    N = 3 * 301
+    ins = [rand(dtype, 4, r, N) for r in range(R)]
+    want = oracle.allreduce(ins, dtype)
+    lens = synth.equal_lengths(N, R)
+    L = P.pl_layout_partitioned(R, lens)
+    pl = plan_for(L, L, "sum", dtype, R, policy(path, form), scratch)
+    outs = [np.zeros(N, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("path,scratch", PATHS)
+@pytest.mark.parametrize("window", WINDOWS)
+def test_alltoall_v(dtype, path, scratch, window):
+    R = 4
+    m = [[(7 * r + 13 * j) % 90 for j in range(R)] for r in range(R)]
+    ins = [rand(dtype, 5, r, sum(m[r])) for r in range(R)]
+    want = oracle.alltoall(ins, m, dtype)
+    lin, lout = P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m)
+    pl = plan_for(lin, lout, "copy", dtype, R, policy(path), scratch)
+    outs = [np.zeros(len(w), NP[dtype]) for w in want]
+    run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
+
+
+@pytest.mark.parametrize("path,scratch", PATHS)
+@pytest.mark.parametrize("window", WINDOWS)
+def test_ulysses(path, scratch, window):
+    R, S, H, D, dtype = 4, 9, 8, 16, "bf16"
+    ins = [rand(dtype, 6, r, S * H * D) for r in range(R)]
+    want = oracle.ulysses_a2a(ins, S, H, D, dtype)
+    lin, lout = P.pl_layout_ulysses_in(R, S, H, D), P.pl_layout_ulysses_out(R, S, H, D)
+    pl = plan_for(lin, lout, "copy", dtype, R, policy(path, chunk=64 * 2), scratch)
+    st = P.pl_plan_get_stats(pl)
+    it, refs, _ = P.pl_plan_get_item(pl, 0)
+    assert it.rows > 1 or st.items >= R * R  # strided rows are kept as rows
+    outs = [np.zeros(len(w), np.uint16) for w in want]
+    run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
+
+
+def test_zero_staging_traffic_is_algorithmic():
+    """ZS plans read and write exactly the algorithmic bytes of each collective."""
+    R, n = 8, 1 << 16
+    S = 2
+    lens = [n] * R
+    ag = plan_for(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy", "bf16", R,
+                  P.pl_policy_default())
+    st = P.pl_plan_get_stats(ag)
+    T = R * n * S
+    assert (st.bytes_read, st.bytes_written) == (T, R * T)
+    L = P.pl_layout_partitioned(R, lens)
+    rs = plan_for(L, P.pl_layout_rank_owned(R, lens), "sum", "bf16", R, P.pl_policy_default())
+    st = P.pl_plan_get_stats(rs)
+    assert (st.bytes_read, st.bytes_written) == (R * T, T)
+    ar = plan_for(L, L, "sum", "bf16", R, P.pl_policy_default())
+    st = P.pl_plan_get_stats(ar)
+    assert (st.bytes_read, st.bytes_written) == (R * T, R * T)
+    assert st.uses_tickets == 0 and st.flags == 0
+
+
+def test_staged_plans_wait_only_on_earlier_items():
+    """Every wait of item j is satisfied by items claimed before j (deadlock freedom)."""
+    R, n = 4, 1000
+    L = P.pl_layout_partitioned(R, [n] * R)
+    pl = plan_for(L, L, "sum", "bf16", R, policy(P.PL_PATH_STAGED, P.PL_AR_COMPOSED), 4 * 2 * 300)
+    st, items = plan_interp.load_plan(pl)
+    notified, credited = {}, {}
+    for j, (it, refs, syncs) in enumerate(items):
+        for s in syncs[:it.nwait]:
+            key = (s.flag, s.use)
+            if s.type == P.PL_SYNC_WAIT_FULL:
+                assert key in notified and notified[key] < j
+            else:
+                assert key in credited and credited[key][0] == credited[key][1]
+        for s in syncs[it.nwait:]:
+            key = (s.flag, s.use)
+            if s.type == P.PL_SYNC_NOTIFY:
+                notified[key] = j
+            else:
+                c = credited.get(key, [0, s.count])
+                credited[key] = [c[0] + 1, s.count]
+    assert st.slots >= 2 and st.uses_tickets == 1
+
+
+def test_invalid_layout_pairs_are_refused():
+    R = 2
+    a = P.pl_layout_create(R, [[(0, 0, 4)], [(1, 0, 4)]])
+    missing = P.pl_layout_create(R, [[(2, 0, 4)], []])
+    short = P.pl_layout_create(R, [[(0, 0, 3)], []])
+    two_on_one = P.pl_layout_create(R, [[(0, 0, 2), (0, 2, 2)], []])
+    for lin, lout, op in ((a, missing, "copy"), (a, short, "copy"), (two_on_one, P.pl_layout_create(R, [[(0, 0, 2)], []]), "sum"),
+                          (P.pl_layout_create(R, [[(0, 0, 4)], [(0, 0, 4)]]), P.pl_layout_create(R, [[(0, 0, 4)], []]), "copy")):
+        with pytest.raises(P.PurlinError) as e:
+            plan_for(lin, lout, op, "fp32", R, None)
+        assert e.value.status == P.PL_ERR_LAYOUT
+    # two strided regions of one name with different row lengths
+    s1 = P.pl_layout_create(1, [[(0, 0, 4, 6, 10)]])
+    s2 = P.pl_layout_create(1, [[(0, 0, 6, 4, 10)]])
+    with pytest.raises(P.PurlinError) as e:
+        plan_for(s1, s2, "copy", "bf16", 1, None)
+    assert e.value.status == P.PL_ERR_UNSUPPORTED
+
+
+def test_layout_arguments_are_checked():
+    with pytest.raises(P.PurlinError):
+        P.pl_layout_create(0, [])
+    with pytest.raises(P.PurlinError):
+        P.pl_layout_create(65, [[]] * 65)
+    with pytest.raises(P.PurlinError):
+        P.pl_layout_create(1, [[(0, 0, 8, 0, 8)]])       # rows = 0
+    with pytest.raises(P.PurlinError):
+        P.pl_layout_create(1, [[(0, 0, 8, 2, 4)]])       # stride < len
+    with pytest.raises(P.PurlinError):
+        P.pl_layout_ulysses_in(3, 4, 8, 2)              # H not a multiple of R
+
+
+def test_staged_needs_a_ring():
+    R = 4
+    L = P.pl_layout_partitioned(R, [1000] * R)
+    with pytest.raises(P.PurlinError) as e:
+        plan_for(L, L, "sum", "bf16", R, policy(P.PL_PATH_STAGED, chunk=1024), scratch=R * 1024)
+    assert e.value.status == P.PL_ERR_NOMEM
