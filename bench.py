@@ -146,6 +146,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time (the job's time) when N replicas run side by side."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(ms_total_max: float, steps: int, T: int, ws: int):
+    """(ms per step, whole-job algbw in GB/s): every replica moves 2*T bytes of
+    collective payload (AllGather + AllReduce) per step."""
+    ms_step = ms_total_max / steps
+    return ms_step, ws * 2 * T / (ms_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------- our arm (GPU)
 
 
@@ -220,7 +238,9 @@ def sampled_parity(wl, device):
 
 
 def time_sweep(ctx, wl, stream, torch):
-    """Latency and algbw per size; sizes below 1 MiB are timed as CUDA graphs of 50 calls."""
+    """Latency and algbw per size.  Up to 64 MiB each point is a CUDA graph of
+    `calls` launches replayed on the launch stream (device time per call, no
+    host launch overhead); above that, events around back-to-back calls."""
     out = []
     for e in range(10, 31):
         T = 1 << e
@@ -233,31 +253,34 @@ def time_sweep(ctx, wl, stream, torch):
             for _ in range(3):
                 fn(ctx, stream.cuda_stream, n)
             torch.cuda.synchronize()
-            if T < (1 << 20):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if T <= (64 << 20):
+                calls = 50 if T <= (4 << 20) else 10
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    for _ in range(50):
+                    for _ in range(calls):
                         fn(ctx, stream.cuda_stream, n)
-                g.replay()
-                torch.cuda.synchronize()
-                reps, calls = 5, 50
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for _ in range(reps):
+                with torch.cuda.stream(stream):
                     g.replay()
-                b.record(stream)
+                    torch.cuda.synchronize()
+                    reps = 5
+                    a.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    b.record(stream)
                 torch.cuda.synchronize()
                 us = a.elapsed_time(b) * 1e3 / (reps * calls)
+                how = "graph"
             else:
-                reps = 20 if T <= (64 << 20) else 5
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 5
                 a.record(stream)
                 for _ in range(reps):
                     fn(ctx, stream.cuda_stream, n)
                 b.record(stream)
                 torch.cuda.synchronize()
                 us = a.elapsed_time(b) * 1e3 / reps
-            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2)}
+                how = "events"
+            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
         out.append(row)
     return out
 
@@ -398,14 +421,8 @@ def run_ours(args):
     ar_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     assert P.pl_ctx_status(ctx, s) == P.PL_OK
 
-    # max over ranks
-    t_max = ms_total
-    if ws > 1:
-        t = torch.tensor([ms_total], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
-    ms_step = t_max / args.steps
-    value = ws * 2 * args.T / (ms_step * 1e-3) / 1e9
+    t_max = max_over_ranks(ms_total, ws, device)
+    ms_step, value = replica_throughput(t_max, args.steps, args.T, ws)
 
     peak, peak_kind = measured_peaks()
     ar_bytes = 2 * R * wl.n_ar * 2        # read R*T, write R*T

@@ -144,6 +144,86 @@ __device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index)
     }
 }
 
+// ------------------------------------------------- bulk-copy (TMA) primitives
+
+constexpr unsigned kBulkPiece = 16384;  // bytes per ring stage
+constexpr unsigned kBulkMin = 4096;     // smaller bodies use the vector path
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Global -> shared bulk copy that completes `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* smem, const void* g, unsigned bytes, unsigned long long* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem)),
+                 "l"(g), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared -> global bulk copy in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* g, const void* smem, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(smem_u32(smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Bounded wait for the phase `parity` of an mbarrier.
+__device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const LaunchArgs& a)
+{
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 255) == 255 && global_ns() - t0 > a.timeout_ns)
+            break;
+    }
+    give_up(a);
+    return false;
+}
+
+// The CTA's bulk-copy ring: `stages` buffers of kBulkPiece bytes, one mbarrier
+// each.  Only thread 0 touches it; `phase` holds the parity each stage's
+// barrier will complete next.
+struct BulkRing {
+    char* buf;
+    unsigned long long* bar;
+    int stages;
+    unsigned phase;
+};
+
 // ------------------------------------------------------------- element math
 
 template <int S> struct Elem;
@@ -340,13 +420,72 @@ __device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigne
     }
 }
 
+// Thread 0: copies `nbytes` (a multiple of 16, both ends 16-byte aligned)
+// from `src` to every destination in `mask` through the ring.  Loads run up
+// to `stages` pieces ahead; a stage is refilled once the stores that read it
+// have finished reading.  Returns with every store complete.
+__device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
+                          const char* src, unsigned nbytes, const LaunchArgs& a)
+{
+    const unsigned np = (nbytes + kBulkPiece - 1) / kBulkPiece;
+    const unsigned st = (unsigned)bk.stages;
+    fence_proxy_async();  // order earlier generic writes (after a flag acquire) before the async loads
+    unsigned issued = 0;
+    auto load = [&](unsigned q) {
+        const unsigned sidx = q % st;
+        const unsigned bytes = min(kBulkPiece, nbytes - q * kBulkPiece);
+        mbar_expect_tx(&bk.bar[sidx], bytes);
+        bulk_g2s(bk.buf + (size_t)sidx * kBulkPiece, src + (size_t)q * kBulkPiece, bytes, &bk.bar[sidx]);
+    };
+    for (; issued < np && issued < st; ++issued)
+        load(issued);
+    bool ok = true;
+    unsigned p = 0;
+    for (; p < np; ++p) {
+        const unsigned sidx = p % st;
+        if (st == 1 && p >= 1) {
+            bulk_wait_read0();
+            load(p);
+            issued = p + 1;
+        }
+        ok = mbar_wait(&bk.bar[sidx], (bk.phase >> sidx) & 1u, a);
+        if (!ok)
+            break;
+        bk.phase ^= 1u << sidx;
+        const unsigned bytes = min(kBulkPiece, nbytes - p * kBulkPiece);
+#pragma unroll 1
+        for (unsigned long long m = mask; m; m &= m - 1) {
+            const int d = __ffsll((long long)m) - 1;
+            bulk_s2g(DST_ROW(sh, d, row) + body + (size_t)p * kBulkPiece, bk.buf + (size_t)sidx * kBulkPiece, bytes);
+        }
+        bulk_commit();
+        if (st > 1 && p >= 1 && issued < np) {
+            bulk_wait_read1();  // the stores of piece p-1 have read their stage
+            load(issued);
+            ++issued;
+        }
+    }
+    if (!ok) {
+        // A load never completed in time: wait (bounded) for every load still in
+        // flight so no copy lands in shared memory after this CTA moves on.
+        for (unsigned q = p; q < issued; ++q) {
+            const unsigned sidx = q % st;
+            if (mbar_wait(&bk.bar[sidx], (bk.phase >> sidx) & 1u, a))
+                bk.phase ^= 1u << sidx;
+        }
+    }
+    bulk_wait_all();
+    fence_proxy_async();  // the async-proxy stores before the generic release that follows
+}
+
 // One row segment of n elements, executed by `nthr` threads with index `tid`.
 // Destinations in `mask` share the same address mod 16 (`dcls`); their
 // stores are 16-byte aligned after a head of at most 16/S - 1 elements, and
 // the rest up to the last whole vector goes through the vector bodies.
-template <int S, int OPS>
+template <int S, int OPS, bool BULK>
 __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                     unsigned n, unsigned dcls, int tid, int nthr)
+                                        unsigned n, unsigned dcls, int tid, int nthr, BulkRing& bk,
+                                        const LaunchArgs& a)
 {
     constexpr int E = 16 / S;
     unsigned head = ((16u - dcls) & 15u) / S;
@@ -383,7 +522,10 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
     for (int s = 0; s < nsrc; ++s)
         aligned &= ((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == 0;
     if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1)) {
-        if (aligned)
+        if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
+            if (tid == 0)
+                bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
+        } else if (aligned)
             copy_body<true>(sh, mask, row, body, nv, tid, nthr);
         else
             copy_body<false>(sh, mask, row, body, nv, tid, nthr);
@@ -398,9 +540,9 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
 // Moves one rows x cols block.  A one-row block is spread over the whole CTA;
 // a multi-row block gives each warp whole rows.  Destinations are grouped by
 // address mod 16; each group is one pass over the sources.
-template <int S, int OPS>
+template <int S, int OPS, bool BULK>
 __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
-                                          unsigned long long cols)
+                                          unsigned long long cols, BulkRing& bk, const LaunchArgs& a)
 {
     const bool one_row = rows == 1;
     const int tid = one_row ? (int)threadIdx.x : (int)(threadIdx.x & 31);
@@ -419,17 +561,27 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
                     group |= 1ull << d;
             }
             todo &= ~group;
-            segment<S, OPS>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr);
+            segment<S, OPS, BULK>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a);
         }
     }
 }
 
 // ------------------------------------------------------------- the kernel
 
-template <int S, int OPS>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid_constant__ LaunchArgs a)
+template <int S, int OPS, bool BULK>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
 {
     __shared__ ItemShared sh;
+    extern __shared__ __align__(128) char dyn[];
+    BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u};
+    if (BULK) {
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < stages; ++i)
+                mbar_init(&bk.bar[i], 1u);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+    }
     __shared__ unsigned s_index;
     __shared__ int s_ok;
     __shared__ Item s_item;
@@ -463,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid
             s_ok = it.nwait ? run_waits(a, it) : 1;
         __syncthreads();
         if (s_ok)
-            move_item<S, OPS>(sh, it.nsrc, it.ndst, it.rows, it.cols);
+            move_item<S, OPS, BULK>(sh, it.nsrc, it.ndst, it.rows, it.cols, bk, a);
         __syncthreads();
         if (tid == 0 && s_ok && it.npost)
             run_posts(a, it, index);
@@ -482,29 +634,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid
 
 }  // namespace
 
+namespace {
+
+template <int S, int OPS, bool BULK>
+cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
+{
+    size_t dyn = BULK ? 128 + (size_t)stages * kBulkPiece : 0;
+    if (BULK) {
+        static bool configured = false;  // per instantiation; the attribute is per function
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(snac_kernel<S, OPS, BULK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)(128 + (size_t)kBulkMaxStages * kBulkPiece));
+            if (e != cudaSuccess)
+                return e;
+            configured = true;
+        }
+    }
+    snac_kernel<S, OPS, BULK><<<ctas, kThreads, dyn, stream>>>(args, stages);
+    return cudaGetLastError();
+}
+
+template <int S, bool BULK>
+cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
+{
+    if (args.ops == kOpsCopy)
+        return launch_one<S, kOpsCopy, BULK>(args, ctas, stages, stream);
+    if (args.ops == kOpsSum)
+        return launch_one<S, kOpsSum, false>(args, ctas, stages, stream);
+    return launch_one<S, kOpsCopy | kOpsSum, BULK>(args, ctas, stages, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream)
 {
-    (void)bulk;
-    (void)stages;
-    const int ops = args.ops;
-#define PL_LAUNCH(SZ, OPS) snac_kernel<SZ, OPS><<<ctas, kThreads, 0, stream>>>(args)
-    if (args.dtype == 0) {
-        if (ops == kOpsCopy)
-            PL_LAUNCH(2, kOpsCopy);
-        else if (ops == kOpsSum)
-            PL_LAUNCH(2, kOpsSum);
-        else
-            PL_LAUNCH(2, kOpsCopy | kOpsSum);
-    } else {
-        if (ops == kOpsCopy)
-            PL_LAUNCH(4, kOpsCopy);
-        else if (ops == kOpsSum)
-            PL_LAUNCH(4, kOpsSum);
-        else
-            PL_LAUNCH(4, kOpsCopy | kOpsSum);
-    }
-#undef PL_LAUNCH
-    return cudaGetLastError();
+    if (stages < 1 || stages > kBulkMaxStages)
+        stages = 4;
+    if (args.dtype == 0)
+        return bulk ? launch_ops<2, true>(args, ctas, stages, stream) : launch_ops<2, false>(args, ctas, stages, stream);
+    return bulk ? launch_ops<4, true>(args, ctas, stages, stream) : launch_ops<4, false>(args, ctas, stages, stream);
 }
 
 int snac_ctas_per_sm(bool bulk, int stages)
@@ -512,7 +680,7 @@ int snac_ctas_per_sm(bool bulk, int stages)
     (void)bulk;
     (void)stages;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum>, kThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum, false>, kThreads, 0) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

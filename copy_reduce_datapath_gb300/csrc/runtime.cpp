@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -45,6 +46,7 @@ uint64_t elem_size(pl_dtype dt) { return dt == PL_BF16 ? 2 : 4; }
 // ------------------------------------------------------------------ layouts
 
 struct pl_layout {
+    uint64_t id = 0;             // unique per created layout (layouts are immutable)
     int R = 0;
     std::vector<int> first;      // R + 1 prefix counts into parts
     std::vector<pl_part> parts;  // contiguous regions normalised to rows = 1
@@ -71,6 +73,8 @@ pl_status make_layout(pl_layout** out, int R, const std::vector<int>& counts, co
     std::unique_ptr<pl_layout> L(new (std::nothrow) pl_layout);
     if (!L)
         return PL_ERR_NOMEM;
+    static std::atomic<uint64_t> next_id{1};
+    L->id = next_id.fetch_add(1);
     L->R = R;
     L->first.assign(R + 1, 0);
     size_t total = 0;
@@ -1023,23 +1027,15 @@ pl_status ensure_flags(pl_ctx* ctx, uint32_t n)
     return PL_OK;
 }
 
+// Layouts are immutable, so a plan is identified by the layouts' ids plus
+// everything else that shapes the work list.
 std::string plan_key(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
                      const ResolvedPolicy& rp)
 {
-    std::string k;
-    auto put = [&](const void* p, size_t n) { k.append((const char*)p, n); };
-    put(&op, sizeof op);
-    put(&dt, sizeof dt);
-    put(&R, sizeof R);
-    put(&rp.path, sizeof rp.path);
-    put(&rp.ar_form, sizeof rp.ar_form);
-    put(&rp.ctas, sizeof rp.ctas);
-    put(&rp.chunk_bytes, sizeof rp.chunk_bytes);
-    for (const pl_layout* L : {&in, &out}) {
-        put(L->first.data(), L->first.size() * sizeof(int));
-        put(L->parts.data(), L->parts.size() * sizeof(pl_part));
-    }
-    return k;
+    uint64_t k[9] = {in.id, out.id, (uint64_t)op, (uint64_t)dt, (uint64_t)R, (uint64_t)rp.path,
+                     (uint64_t)rp.ar_form, ((uint64_t)rp.ctas << 32) | (uint64_t)(rp.datapath == PL_ATOM_BULK),
+                     rp.chunk_bytes};
+    return std::string(reinterpret_cast<const char*>(k), sizeof k);
 }
 
 pl_status get_plan(pl_ctx* ctx, const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,

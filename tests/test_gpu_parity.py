@@ -370,3 +370,54 @@ def test_dropped_notify_times_out_and_recovers(ctx):
     want = oracle.allreduce(ins, dtype)
     for r in range(R):
         assert_equal(to_np(outs[r], dtype), want[r], f"rank {r}")
+
+
+# ------------------------------------------------- bulk-copy ring datapath
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 8])
+def test_bulk_ring_datapath(ctx, stages):
+    """The cp.async.bulk shared-memory ring (1..8 stages) on aligned copies; the
+    unaligned V forms and strided rows fall back to the vector path."""
+    R, dtype = 8, "bf16"
+    pol = P.pl_policy_default(datapath=P.PL_ATOM_BULK, stages=stages)
+    n = (1 << 20) // 2 // R + 8  # a piece count that does not divide evenly
+    ins = [host("normal", dtype, 17, r, n) for r in range(R)]
+    got = run(ctx, P.pl_layout_rank_owned(R, [n] * R), P.pl_layout_partitioned(R, [n] * R), "copy", dtype, ins,
+              [n * R] * R, pol)
+    want = oracle.allgather(ins, dtype)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"AG rank {r}")
+    m = [[(n // R) + 3 * ((r + j) % 2) for j in range(R)] for r in range(R)]
+    ains = [host("normal", dtype, 18, r, sum(m[r])) for r in range(R)]
+    outn = [sum(m[r][j] for r in range(R)) for j in range(R)]
+    got = run(ctx, P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), "copy", dtype, ains, outn, pol)
+    want = oracle.alltoall(ains, m, dtype)
+    for j in range(R):
+        assert_equal(got[j], want[j], f"A2A rank {j}")
+    S, H, D = 64, 32, 128
+    uins = [host("normal", dtype, 19, r, S * H * D) for r in range(R)]
+    got = run(ctx, P.pl_layout_ulysses_in(R, S, H, D), P.pl_layout_ulysses_out(R, S, H, D), "copy", dtype, uins,
+              [S * H * D] * R, pol)
+    want = oracle.ulysses_a2a(uins, S, H, D, dtype)
+    for j in range(R):
+        assert_equal(got[j], want[j], f"Ulysses rank {j}")
+
+
+@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
+def test_bulk_ring_in_flagged_paths(ctx, form):
+    """Bulk copies inside staged and composed plans (stage, gather) with flags."""
+    R, n, dtype = 8, 1 << 18, "bf16"
+    ins = [host("normal", dtype, 20, r, n) for r in range(R)]
+    want = oracle.allreduce(ins, dtype)
+    for path in (P.PL_PATH_ZS, P.PL_PATH_STAGED):
+        pol = P.pl_policy_default(datapath=P.PL_ATOM_BULK, stages=4, path=path, allreduce_form=form,
+                                  chunk_bytes=64 << 10)
+        dev = [to_dev(a, dtype) for a in ins]
+        outs = Outs([n] * R, dtype)
+        s = P.stream_handle()
+        P.pl_allreduce(ctx, dtype, R, n, P.ptrs(dev), outs.ptrs(), pol, s)
+        assert P.pl_ctx_status(ctx, s) == P.PL_OK
+        outs.check_guards()
+        for r in range(R):
+            assert_equal(outs.host(r), want[r], f"path {path} rank {r}")
