@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
           f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["runtime.cpp", "atom.cu"]
+SOURCES = ["runtime.cpp", "atom.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:

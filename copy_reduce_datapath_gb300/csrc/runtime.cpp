@@ -1318,3 +1318,45 @@ PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dt, int R, uint64_t count, v
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ caller-memory work lists
+
+namespace purlin {
+
+int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bufs, void* const* out_bufs,
+                            int num_sms, uint64_t ring_bytes, uint64_t chunk_bytes, HostWorkList& out)
+{
+    if (R < 1 || R > kMaxRanks || !in_bufs || !out_bufs || (dtype != PL_BF16 && dtype != PL_FP32))
+        return PL_ERR_INVALID;
+    std::vector<uint64_t> lens(R, count / (uint64_t)R);
+    lens[R - 1] = count - (count / (uint64_t)R) * (uint64_t)(R - 1);
+    pl_layout* L = nullptr;
+    pl_status st = pl_layout_partitioned(&L, R, lens.data());
+    if (st != PL_OK)
+        return st;
+    std::unique_ptr<pl_layout> hold(L);
+    std::vector<uint64_t> counts(R, count);
+    if ((st = check_buffers(*L, *L, (pl_dtype)dtype, R, in_bufs, counts.data(), out_bufs, counts.data())) != PL_OK)
+        return st;
+    pl_policy pol;
+    pl_policy_default(&pol);
+    pol.path = PL_PATH_STAGED;
+    pol.allreduce_form = PL_AR_FUSED;
+    pol.chunk_bytes = chunk_bytes;
+    ResolvedPolicy rp;
+    if ((st = resolve_policy(&pol, rp)) != PL_OK)
+        return st;
+    HostPlan hp;
+    if ((st = derive(*L, *L, PL_SUM, (pl_dtype)dtype, R, rp, num_sms, kDefaultCtasPerSm, ring_bytes, hp)) != PL_OK)
+        return st;
+    out.items = std::move(hp.items);
+    out.refs = std::move(hp.refs);
+    out.syncs = std::move(hp.syncs);
+    out.nflags = hp.nflags;
+    out.ops = hp.ops;
+    out.ctas = hp.stats.ctas;
+    out.uses_tickets = hp.stats.uses_tickets;
+    return PL_OK;
+}
+
+}  // namespace purlin

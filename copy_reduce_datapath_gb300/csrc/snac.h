@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -95,5 +96,23 @@ cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages,
 
 // CTAs of the SNAC kernel that fit on one SM at once.
 int snac_ctas_per_sm(bool bulk, int stages);
+
+// Host-side work list of a staged AllReduce whose device state lives in
+// caller-provided memory (runtime.cpp; used by the allocation-free entry point).
+struct HostWorkList {
+    std::vector<Item> items;
+    std::vector<Ref> refs;
+    std::vector<Sync> syncs;
+    uint32_t nflags = 0;
+    int ops = 0;
+    int ctas = 1;
+    int uses_tickets = 0;
+};
+
+// Validates the buffers like pl_allreduce and derives the staged, fused
+// AllReduce of `count` elements per rank over a ring of `ring_bytes` with
+// chunks of `chunk_bytes`.  Host memory only; no CUDA call.
+int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bufs, void* const* out_bufs,
+                            int num_sms, uint64_t ring_bytes, uint64_t chunk_bytes, HostWorkList& out);
 
 }  // namespace purlin

@@ -102,6 +102,7 @@ def _load():
         "pl_collective": (i32, [vp, vp, vp, i32, i32, C.c_int, vpp, u64p, vpp, u64p,
                                 C.POINTER(pl_policy), vp]),
         "pl_allreduce": (i32, [vp, i32, C.c_int, u64, vpp, vpp, C.POINTER(pl_policy), vp]),
+        "pl_allreduce_noalloc": (i32, [i32, C.c_int, u64, vpp, vpp, C.c_int, vp]),
         "pl_plan_create": (i32, [vpp, vp, vp, i32, i32, C.c_int, C.POINTER(pl_policy), C.c_int, u64]),
         "pl_plan_destroy": (i32, [vp]),
         "pl_plan_get_stats": (i32, [vp, C.POINTER(pl_plan_stats)]),
@@ -275,6 +276,14 @@ def pl_allreduce(ctx, dtype, R, count, in_ptrs, out_ptrs, policy: pl_policy | No
     st = lib.pl_allreduce(ctx, _dtype(dtype), R, count, _ptrs(in_ptrs), _ptrs(out_ptrs),
                           C.byref(policy) if policy is not None else None, stream or None)
     _check(st, "pl_allreduce")
+
+
+def pl_allreduce_noalloc(dtype, R, count, in_ptrs, out_ptrs, wait: bool = True, stream: int = 0) -> int:
+    """AllReduce that allocates no device memory (its state lives in the
+    library's static device array).  Returns the pl_status: with wait=True it
+    also waits for `stream` and reports a device-side timeout."""
+    return lib.pl_allreduce_noalloc(_dtype(dtype), R, count, _ptrs(in_ptrs), _ptrs(out_ptrs), 1 if wait else 0,
+                                    stream or None)
 
 
 # ------------------------------------------------------- plan introspection

@@ -219,6 +219,33 @@ PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dtype, int R, uint64_t count
                               void* const* in_bufs, void* const* out_bufs,
                               const pl_policy* policy, void* stream);
 
+/* AllReduce that allocates no device memory.  The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- a process
+ * that reserves its device memory budget once at start-up and may not grow it,
+ * a plug-in that does not own the process's device allocator, or code on a
+ * latency path where an allocation (which can synchronise the device) is not
+ * acceptable.  The result is the same as pl_allreduce with a staged policy:
+ * out_bufs[r][i] = rank-ordered fp32 sum over ranks of in_bufs[*][i], rounded
+ * once to dtype, for every r (out_bufs may equal in_bufs).
+ *
+ * No context: the flag words, the derived work list and the staging ring live
+ * in one file-scope device array of 32 MiB that every GPU loading the library
+ * holds until the process exits.  Limits: R <= 8 and count * element size
+ * <= 256 MiB per rank; larger requests return PL_ERR_NOMEM before anything
+ * runs.  Buffer errors return PL_ERR_INVALID / PL_ERR_ALIAS like pl_allreduce.
+ *
+ * The call works on the current CUDA device.  Its first call on a device also
+ * looks up the array's device address there (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Every call clears the array's flag
+ * words and copies its work list into the array on `stream` before launching
+ * one kernel there, so calls issued in order on one stream are safe, while
+ * calls whose work overlaps on the GPU (other streams, other threads) share
+ * the array and race.  wait = 0 returns once the work is queued; wait != 0
+ * also waits for `stream` and returns the device status (PL_OK, or
+ * PL_ERR_TIMEOUT if a bounded wait expired). */
+PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t count, void* const* in_bufs,
+                                      void* const* out_bufs, int wait, void* stream);
+
 /* ----------------------------------------------------- plan introspection */
 
 /* The SNAC work list derived from a layout pair (abstract: orchestration
