@@ -374,7 +374,7 @@ template <int S, bool QALIGNED>
 __device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                       size_t body, unsigned nv, int tid, int nthr)
 {
-    constexpr int G = QALIGNED ? 8 : 4;
+    constexpr int G = QALIGNED ? 8 : 1;
     for (unsigned v = tid; v < nv; v += nthr) {
         Acc<S> acc;
         for (int s0 = 0; s0 < nsrc; s0 += G) {
@@ -478,11 +478,146 @@ __device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long
     fence_proxy_async();  // the async-proxy stores before the generic release that follows
 }
 
+// Every source of the segment sits the same q bytes (q != 0) past a 16-byte
+// boundary while the destinations are 16-byte aligned at `body`.  Each warp
+// step loads 32 consecutive aligned vectors of every source (one per lane),
+// adds them lane by lane (sum), and lanes 0..30 splice their result with the
+// next lane's into one destination vector: 31 outputs per 32 loaded vectors,
+// one load per source per vector and one realignment per output.  Aligned
+// vector nv is the last one that holds bytes of the row.
+template <int S, bool SUM>
+__device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                             size_t body, unsigned nv, int q, int tid, int nthr)
+{
+    constexpr int U = SUM ? 2 : 8;  // warp steps in flight per thread
+    constexpr int G = 4;            // sources in flight per step (sum)
+    const int lane = tid & 31;
+    const unsigned warp = (unsigned)tid >> 5;
+    const unsigned span = 31u * ((unsigned)nthr >> 5);
+    for (unsigned g0 = warp * 31u; g0 < nv; g0 += span * U) {
+        uint4 r[U];
+        if constexpr (!SUM) {
+            const char* base = SRC_ROW(sh, 0, row) + body - q;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned idx = g0 + u * span + lane;
+                r[u] = idx <= nv ? ld16(base + (size_t)idx * 16) : make_uint4(0, 0, 0, 0);
+            }
+        } else {
+            Acc<S> acc[U];
+            for (int s0 = 0; s0 < nsrc; s0 += G) {
+                uint4 x[U][G];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned idx = g0 + u * span + lane;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        x[u][g] = (s0 + g < nsrc && idx <= nv)
+                                      ? ld16(SRC_ROW(sh, s0 + g, row) + body - q + (size_t)idx * 16)
+                                      : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (s0 + g < nsrc) {
+                            if (s0 + g == 0)
+                                acc[u].set(x[u][g]);
+                            else
+                                acc[u].add(x[u][g]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                r[u] = acc[u].pack();
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint4 nb;
+            nb.x = __shfl_down_sync(0xffffffffu, r[u].x, 1);
+            nb.y = __shfl_down_sync(0xffffffffu, r[u].y, 1);
+            nb.z = __shfl_down_sync(0xffffffffu, r[u].z, 1);
+            nb.w = __shfl_down_sync(0xffffffffu, r[u].w, 1);
+            const unsigned out = g0 + u * span + lane;
+            if (lane < 31 && out < nv) {
+                const uint4 v = realign(r[u], nb, q);
+#pragma unroll 1
+                for (unsigned long long m = mask; m; m &= m - 1) {
+                    const int d = __ffsll((long long)m) - 1;
+                    st16(DST_ROW(sh, d, row) + body + (size_t)out * 16, v);
+                }
+            }
+        }
+    }
+}
+
+// A multi-row block whose rows are whole 16-byte vectors at 16-byte aligned
+// addresses in every source and destination: one flat index over
+// rows x vectors-per-row spread over the whole CTA (no per-row heads, tails
+// or realignment).
+template <int S, bool SUM>
+__device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int ndst, unsigned rows, unsigned vpr,
+                                            int tid, int nthr)
+{
+    const unsigned total = rows * vpr;
+    if constexpr (!SUM) {
+        constexpr int U = 8;
+        for (unsigned v0 = tid; v0 < total; v0 += (unsigned)nthr * U) {
+            uint4 x[U];
+            unsigned rr[U], cc[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
+                rr[u] = v / vpr;
+                cc[u] = v - rr[u] * vpr;
+                if (v < total)
+                    x[u] = ld16(SRC_ROW(sh, 0, rr[u]) + (size_t)cc[u] * 16);
+            }
+#pragma unroll 1
+            for (int d = 0; d < ndst; ++d) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (v0 + u * nthr < total)
+                        st16(DST_ROW(sh, d, rr[u]) + (size_t)cc[u] * 16, x[u]);
+            }
+        }
+    } else {
+        constexpr int G = 8;
+        for (unsigned v = tid; v < total; v += nthr) {
+            const unsigned rr = v / vpr;
+            const unsigned cc = v - rr * vpr;
+            Acc<S> acc;
+            for (int s0 = 0; s0 < nsrc; s0 += G) {
+                uint4 x[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (s0 + g < nsrc)
+                        x[g] = ld16(SRC_ROW(sh, s0 + g, rr) + (size_t)cc * 16);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (s0 + g < nsrc) {
+                        if (s0 + g == 0)
+                            acc.set(x[g]);
+                        else
+                            acc.add(x[g]);
+                    }
+                }
+            }
+            const uint4 out = acc.pack();
+#pragma unroll 1
+            for (int d = 0; d < ndst; ++d)
+                st16(DST_ROW(sh, d, rr) + (size_t)cc * 16, out);
+        }
+    }
+}
+
 // One row segment of n elements, executed by `nthr` threads with index `tid`.
 // Destinations in `mask` share the same address mod 16 (`dcls`); their
 // stores are 16-byte aligned after a head of at most 16/S - 1 elements, and
 // the rest up to the last whole vector goes through the vector bodies.
-template <int S, int OPS, bool BULK>
+template <int S, int OPS, bool BULK, bool ALIGN>
 __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                         unsigned n, unsigned dcls, int tid, int nthr, BulkRing& bk,
                                         const LaunchArgs& a)
@@ -491,11 +626,19 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
     unsigned head = ((16u - dcls) & 15u) / S;
     if (head > n)
         head = n;
-    const unsigned nv = (n - head) / E;
+    unsigned nv = (n - head) / E;
+    if (ALIGN) {
+        // Kernels built for plans the host proved 16-byte aligned have no
+        // realigning bodies; should a segment still be misaligned, it is moved
+        // element by element below (correct, slower).
+        for (int s = 0; s < nsrc; ++s)
+            if (((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + (size_t)head * S) & 15u) != 0)
+                nv = 0;
+    }
     const unsigned tail0 = head + nv * E;
     const unsigned ntail = n - tail0;
 
-    // Scalar head and tail elements.
+    // Scalar head and tail elements (and, see above, misaligned rows of aligned kernels).
     for (unsigned e = tid; e < head + ntail; e += nthr) {
         const unsigned i = e < head ? e : tail0 + (e - head);
         uint32_t v;
@@ -518,20 +661,25 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         return;
 
     const size_t body = (size_t)head * S;
-    bool aligned = true;
-    for (int s = 0; s < nsrc; ++s)
-        aligned &= ((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == 0;
+    // Misalignment of every source relative to the aligned destinations.
+    const int q0 = (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, 0, row)) + body) & 15u);
+    bool uniform = true;
+    for (int s = 1; s < nsrc; ++s)
+        uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
+    const bool aligned = uniform && q0 == 0;
     if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1)) {
         if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
             if (tid == 0)
                 bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
-        } else if (aligned)
+        } else if (ALIGN || aligned)
             copy_body<true>(sh, mask, row, body, nv, tid, nthr);
         else
-            copy_body<false>(sh, mask, row, body, nv, tid, nthr);
+            shifted_body<S, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
     } else if (OPS & kOpsSum) {
-        if (aligned)
+        if (ALIGN || aligned)
             sum_body<S, true>(sh, nsrc, mask, row, body, nv, tid, nthr);
+        else if (uniform)
+            shifted_body<S, true>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
         else
             sum_body<S, false>(sh, nsrc, mask, row, body, nv, tid, nthr);
     }
@@ -540,10 +688,26 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
 // Moves one rows x cols block.  A one-row block is spread over the whole CTA;
 // a multi-row block gives each warp whole rows.  Destinations are grouped by
 // address mod 16; each group is one pass over the sources.
-template <int S, int OPS, bool BULK>
+template <int S, int OPS, bool BULK, bool ALIGN>
 __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
                                           unsigned long long cols, BulkRing& bk, const LaunchArgs& a)
 {
+    if (rows > 1 && ((cols * S) & 15u) == 0) {
+        // Rows of whole vectors, every row start aligned in every reference?
+        bool flat = true;
+        for (int i = 0; i < nsrc; ++i)
+            flat &= ((reinterpret_cast<uintptr_t>(sh.src[i]) | sh.sstride[i]) & 15u) == 0;
+        for (int i = 0; i < ndst; ++i)
+            flat &= ((reinterpret_cast<uintptr_t>(sh.dst[i]) | sh.dstride[i]) & 15u) == 0;
+        if (flat) {
+            const unsigned vpr = (unsigned)(cols * S / 16);
+            if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1))
+                flat2d_body<S, false>(sh, 1, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
+            else if (OPS & kOpsSum)
+                flat2d_body<S, true>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
+            return;
+        }
+    }
     const bool one_row = rows == 1;
     const int tid = one_row ? (int)threadIdx.x : (int)(threadIdx.x & 31);
     const int nthr = one_row ? (int)blockDim.x : 32;
@@ -561,61 +725,114 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
                     group |= 1ull << d;
             }
             todo &= ~group;
-            segment<S, OPS, BULK>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a);
+            segment<S, OPS, BULK, ALIGN>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a);
         }
     }
 }
 
 // ------------------------------------------------------------- the kernel
 
-template <int S, int OPS, bool BULK>
+// Shared-memory image of one claimed work item: its index and its header.
+struct Slot {
+    unsigned index;
+    Item item;
+};
+
+// Thread 0: the next item index of this CTA (in index order through the
+// device ticket when items wait on one another, else round-robin).
+__device__ __forceinline__ unsigned claim(const LaunchArgs& a, unsigned k)
+{
+    return a.use_tickets ? atomicAdd(a.st.ticket, 1u) : blockIdx.x + k * gridDim.x;
+}
+
+// Region pointer of reference `tid` of `it` into `sh`.
+template <int S>
+__device__ __forceinline__ void put_ref(const LaunchArgs& a, const Item& it, const Ref& f, ItemShared& sh, int tid)
+{
+    char* base = a.bufs[f.buf] + f.offset * (unsigned long long)S;
+    const unsigned long long stride = f.stride * (unsigned long long)S;
+    if (tid < it.nsrc) {
+        sh.src[tid] = base;
+        sh.sstride[tid] = stride;
+    } else {
+        sh.dst[tid - it.nsrc] = base;
+        sh.dstride[tid - it.nsrc] = stride;
+    }
+}
+
+// The persistent SNAC kernel.  While item k moves, the region references of
+// item k+1 and the header of item k+2 are already in flight, so the work
+// list's metadata adds no round trips per item.  With tickets, a CTA holds
+// at most two claimed items and processes them in claim order; every wait of
+// an item refers to items with smaller indices, held by running CTAs, so the
+// grid always progresses.  A CTA claims item k+2 only while item k+1 exists,
+// so every CTA makes exactly one claim beyond the end of the list.
+template <int S, int OPS, bool BULK, bool ALIGN>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
 {
-    __shared__ ItemShared sh;
+    __shared__ ItemShared sh[2];
+    __shared__ Slot slot[2];
+    __shared__ int s_ok;
     extern __shared__ __align__(128) char dyn[];
     BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u};
-    if (BULK) {
-        if (threadIdx.x == 0) {
+    const int tid = (int)threadIdx.x;
+    if (tid == 0) {
+        if (BULK) {
             for (int i = 0; i < stages; ++i)
                 mbar_init(&bk.bar[i], 1u);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
-        __syncthreads();
+        const unsigned i0 = claim(a, 0);
+        const unsigned i1 = i0 < a.nitems ? claim(a, 1) : ~0u;
+        // both header loads in flight before either is stored
+        Item h0{}, h1{};
+        if (i0 < a.nitems)
+            h0 = a.items[i0];
+        if (i1 < a.nitems)
+            h1 = a.items[i1];
+        slot[0].index = i0;
+        slot[1].index = i1;
+        slot[0].item = h0;
+        slot[1].item = h1;
     }
-    __shared__ unsigned s_index;
-    __shared__ int s_ok;
-    __shared__ Item s_item;
-    const int tid = (int)threadIdx.x;
+    __syncthreads();
+    if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
+        put_ref<S>(a, slot[0].item, a.refs[slot[0].item.ref + tid], sh[0], tid);
+    __syncthreads();
 
     for (unsigned k = 0;; ++k) {
-        if (tid == 0) {
-            s_index = a.use_tickets ? atomicAdd(a.st.ticket, 1u) : blockIdx.x + k * gridDim.x;
-            if (s_index < a.nitems)
-                s_item = a.items[s_index];
-        }
-        __syncthreads();
-        const unsigned index = s_index;
+        const int cur = (int)(k & 1u), nxt = cur ^ 1;
+        const unsigned index = slot[cur].index;
         if (index >= a.nitems)
             break;
-        const Item it = s_item;
-        const int nref = it.nsrc + it.ndst;
-        if (tid < nref) {
-            const Ref f = a.refs[it.ref + tid];
-            char* base = a.bufs[f.buf] + f.offset * (unsigned long long)S;
-            const unsigned long long stride = f.stride * (unsigned long long)S;
-            if (tid < it.nsrc) {
-                sh.src[tid] = base;
-                sh.sstride[tid] = stride;
-            } else {
-                sh.dst[tid - it.nsrc] = base;
-                sh.dstride[tid - it.nsrc] = stride;
+        const Item it = slot[cur].item;
+        const unsigned next_index = slot[nxt].index;
+        // This thread's reference of item k+1: loaded now, stored after the move.
+        const Item nit = slot[nxt].item;
+        const bool has_ref = next_index < a.nitems && tid < nit.nsrc + nit.ndst;
+        Ref nref{};
+        if (has_ref)
+            nref = a.refs[nit.ref + tid];
+        unsigned i2 = ~0u;
+        Item h2{};
+        if (tid == 0) {
+            if (next_index < a.nitems) {
+                i2 = claim(a, k + 2);
+                if (i2 < a.nitems)
+                    h2 = a.items[i2];
             }
-        }
-        if (tid == 0)
             s_ok = it.nwait ? run_waits(a, it) : 1;
+        }
         __syncthreads();
         if (s_ok)
-            move_item<S, OPS, BULK>(sh, it.nsrc, it.ndst, it.rows, it.cols, bk, a);
+            move_item<S, OPS, BULK, ALIGN>(sh[cur], it.nsrc, it.ndst, it.rows, it.cols, bk, a);
+        if (has_ref)
+            put_ref<S>(a, nit, nref, sh[nxt], tid);  // sh[nxt] served item k-1, done before the last barrier
+        if (tid == 0) {
+            // every thread read slot[cur] and slot[nxt] before the barrier above
+            slot[cur].index = i2;
+            slot[cur].item = h2;
+        }
         __syncthreads();
         if (tid == 0 && s_ok && it.npost)
             run_posts(a, it, index);
@@ -636,32 +853,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid
 
 namespace {
 
-template <int S, int OPS, bool BULK>
+template <int S, int OPS, bool BULK, bool ALIGN>
 cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
 {
     size_t dyn = BULK ? 128 + (size_t)stages * kBulkPiece : 0;
     if (BULK) {
         static bool configured = false;  // per instantiation; the attribute is per function
         if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(snac_kernel<S, OPS, BULK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(snac_kernel<S, OPS, BULK, ALIGN>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)(128 + (size_t)kBulkMaxStages * kBulkPiece));
             if (e != cudaSuccess)
                 return e;
             configured = true;
         }
     }
-    snac_kernel<S, OPS, BULK><<<ctas, kThreads, dyn, stream>>>(args, stages);
+    snac_kernel<S, OPS, BULK, ALIGN><<<ctas, kThreads, dyn, stream>>>(args, stages);
     return cudaGetLastError();
 }
 
-template <int S, bool BULK>
+template <int S, bool BULK, bool ALIGN>
 cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
 {
     if (args.ops == kOpsCopy)
-        return launch_one<S, kOpsCopy, BULK>(args, ctas, stages, stream);
+        return launch_one<S, kOpsCopy, BULK, ALIGN>(args, ctas, stages, stream);
     if (args.ops == kOpsSum)
-        return launch_one<S, kOpsSum, false>(args, ctas, stages, stream);
-    return launch_one<S, kOpsCopy | kOpsSum, BULK>(args, ctas, stages, stream);
+        return launch_one<S, kOpsSum, false, ALIGN>(args, ctas, stages, stream);
+    return launch_one<S, kOpsCopy | kOpsSum, BULK, ALIGN>(args, ctas, stages, stream);
+}
+
+template <int S>
+cudaError_t launch_dtype(const LaunchArgs& args, int ctas, bool bulk, bool aligned, int stages, cudaStream_t stream)
+{
+    if (bulk)
+        return aligned ? launch_ops<S, true, true>(args, ctas, stages, stream)
+                       : launch_ops<S, true, false>(args, ctas, stages, stream);
+    return aligned ? launch_ops<S, false, true>(args, ctas, stages, stream)
+                   : launch_ops<S, false, false>(args, ctas, stages, stream);
 }
 
 }  // namespace
@@ -670,9 +898,14 @@ cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages,
 {
     if (stages < 1 || stages > kBulkMaxStages)
         stages = 4;
+    // A plan whose every reference is 16-byte aligned, over 16-byte aligned
+    // buffers, runs in the instantiation without realigning bodies.
+    bool aligned = args.all_aligned != 0;
+    for (int i = 0; aligned && i < args.nbufs; ++i)
+        aligned = (reinterpret_cast<uintptr_t>(args.bufs[i]) & 15u) == 0;
     if (args.dtype == 0)
-        return bulk ? launch_ops<2, true>(args, ctas, stages, stream) : launch_ops<2, false>(args, ctas, stages, stream);
-    return bulk ? launch_ops<4, true>(args, ctas, stages, stream) : launch_ops<4, false>(args, ctas, stages, stream);
+        return launch_dtype<2>(args, ctas, bulk, aligned, stages, stream);
+    return launch_dtype<4>(args, ctas, bulk, aligned, stages, stream);
 }
 
 int snac_ctas_per_sm(bool bulk, int stages)
@@ -680,7 +913,7 @@ int snac_ctas_per_sm(bool bulk, int stages)
     (void)bulk;
     (void)stages;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum, false>, kThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum, false, false>, kThreads, 0) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

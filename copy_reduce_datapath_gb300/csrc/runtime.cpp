@@ -34,6 +34,7 @@ namespace {
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr uint64_t kMinChunkBytes = 8 << 10;
 constexpr uint64_t kMaxChunkBytes = 4 << 20;
+constexpr uint64_t kTicketedChunkBytes = 256 << 10;
 constexpr int kItemsPerCta = 4;       // auto chunking aims at this many items per CTA
 constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threads x 128 registers)
 constexpr size_t kMaxCachedPlans = 1024;
@@ -345,7 +346,9 @@ struct HostPlan {
     std::vector<Ref> refs;
     std::vector<Sync> syncs;
     uint32_t nflags = 0;
-    int ops = 0;  // kOpsCopy | kOpsSum
+    int lag = 0;          // chunk rows between producers and their consumers in claim order
+    int ops = 0;          // kOpsCopy | kOpsSum
+    int all_aligned = 0;  // every reference's byte offset and row stride is a multiple of 16
     pl_plan_stats stats{};
 };
 
@@ -576,8 +579,11 @@ bool waits_precede(const HostPlan& hp)
     return true;
 }
 
-pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
-                 const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, HostPlan& hp)
+// Derives the work list with consumers emitted `lag` chunk rows behind the
+// producers they wait for (so the CTAs that claim them in order rarely spin).
+pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                       const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, int lag,
+                       HostPlan& hp)
 {
     if (in.R != R || out.R != R)
         return PL_ERR_INVALID;
@@ -607,6 +613,15 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
     chunk_bytes = std::max<uint64_t>(256, chunk_bytes / 256 * 256);
 
     const bool staged = pol.path == PL_PATH_STAGED;
+    // Plans whose items wait on one another keep about one grid of chunks in
+    // flight between a producer and its consumers; small chunks keep those
+    // bytes resident in L2, so consumers read them from there.
+    bool multi_dst_sum = false;
+    for (const Transfer& t : ts)
+        multi_dst_sum |= op == PL_SUM && t.srcs.size() > 1 && t.dsts.size() > 1;
+    const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
+    if (ticketed && pol.chunk_bytes == 0)
+        chunk_bytes = std::min<uint64_t>(chunk_bytes, kTicketedChunkBytes);
     if (staged && pol.chunk_bytes == 0) {
         uint64_t per_rank = scratch_bytes / (uint64_t)R;
         chunk_bytes = std::min(chunk_bytes, std::max<uint64_t>(256, per_rank / 4 / 256 * 256));
@@ -633,6 +648,16 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
     }
 
     Builder b(hp, R);
+    struct Deferred {
+        Builder::Pending p;
+        ItemKind kind;
+        pl_op op;
+        Chunk ch;
+    };
+    // phase 0: producers (zero-staging moves, stages, owner reduce of the
+    // zero-staging composed form); phase 1: consumers of staged chunks;
+    // phase 2: gathers of reduced chunks.
+    std::vector<std::vector<Deferred>> rows[3];
     bool tickets = false;
     uint32_t next_flag = 0;
     // staged ring bookkeeping
@@ -658,6 +683,14 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
         return PL_OK;
     };
 
+    for (auto& r : rows)
+        r.assign(max_chunks, {});
+    auto put = [&](size_t row, int phase, Builder::Pending& pend, ItemKind kind, pl_op pop, const Chunk& ch) {
+        if (lag == 0 || !ticketed)
+            b.emit(pend, kind, pop, ch);  // creation order: each transfer's producers, then its consumers
+        else
+            rows[phase][row].push_back(Deferred{std::move(pend), kind, pop, ch});
+    };
     for (size_t c = 0; c < max_chunks; ++c) {
         for (size_t ti = 0; ti < ts.size(); ++ti) {
             if (c >= chunks[ti].size())
@@ -679,7 +712,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                         red.src.push_back(b.region(g, ch));
                     red.dst.push_back(b.region(t.dsts[o], ch));
                     red.posts.push_back(mk_sync(kNotify, flag, 0));
-                    b.emit(red, kMove, op, ch);
+                    put(c, 0, red, kMove, op, ch);
                     bytes_read += blk * t.srcs.size();
                     bytes_written += blk;
                     for (size_t d = 0; d < t.dsts.size(); ++d) {
@@ -689,7 +722,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                         ag.src.push_back(b.region(t.dsts[o], ch));
                         ag.dst.push_back(b.region(t.dsts[d], ch));
                         ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
-                        b.emit(ag, kConsume, PL_COPY, ch);
+                        put(c, 2, ag, kConsume, PL_COPY, ch);
                         bytes_read += blk;
                         bytes_written += blk;
                     }
@@ -702,7 +735,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                         size_t d1 = std::min(t.dsts.size(), d0 + kMaxRanks);
                         for (size_t d = d0; d < d1; ++d)
                             mv.dst.push_back(b.region(t.dsts[d], ch));
-                        b.emit(mv, kMove, op, ch);
+                        put(c, 0, mv, kMove, op, ch);
                         bytes_read += blk * t.srcs.size();
                         bytes_written += blk * (d1 - d0);
                     }
@@ -724,7 +757,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                 if (use[s] > 0)
                     sg.waits.push_back(mk_sync(kWaitFree, slot[s], use[s] - 1));
                 sg.posts.push_back(mk_sync(kNotify, slot[s], use[s]));
-                b.emit(sg, kStage, PL_COPY, ch);
+                put(c, 0, sg, kStage, PL_COPY, ch);
                 bytes_read += blk;
                 bytes_written += blk;
             }
@@ -737,7 +770,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                     cs.dst.push_back(b.region(t.dsts[d], ch));
                     cs.waits.push_back(mk_sync(kWaitFull, slot[0], use[0]));
                     cs.posts.push_back(mk_sync(kCredit, slot[0], use[0], n));
-                    b.emit(cs, kConsume, PL_COPY, ch);
+                    put(c, 1, cs, kConsume, PL_COPY, ch);
                     bytes_read += blk;
                     bytes_written += blk;
                 }
@@ -752,7 +785,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                     cs.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
                     cs.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
                 }
-                b.emit(cs, kConsume, op, ch);
+                put(c, 1, cs, kConsume, op, ch);
                 bytes_read += blk * t.srcs.size();
                 bytes_written += blk * t.dsts.size();
             } else {
@@ -774,7 +807,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                 for (size_t s = 0; s < t.srcs.size(); ++s)
                     red.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
                 red.posts.push_back(mk_sync(kNotify, yslot, yuse));
-                b.emit(red, kConsume, op, ch);
+                put(c, 1, red, kConsume, op, ch);
                 bytes_read += blk * t.srcs.size();
                 bytes_written += 2 * blk;
                 uint32_t n = (uint32_t)t.dsts.size() - 1;
@@ -786,7 +819,7 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
                     ag.dst.push_back(b.region(t.dsts[d], ch));
                     ag.waits.push_back(mk_sync(kWaitFull, yslot, yuse));
                     ag.posts.push_back(mk_sync(kCredit, yslot, yuse, n));
-                    b.emit(ag, kConsume, PL_COPY, ch);
+                    put(c, 2, ag, kConsume, PL_COPY, ch);
                     bytes_read += blk;
                     bytes_written += blk;
                 }
@@ -794,13 +827,45 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
         }
     }
 
+    // Emit: producers of row t, their consumers L rows later, gathers of
+    // reduced chunks one more lag later (or L when nothing sits between).
+    // The automatic lag puts about one grid of items between a producer and
+    // its first consumer, so consumers are claimed once producers are done.
+    if (lag < 0 && max_chunks > 0) {
+        size_t per_row = std::max<size_t>(1, rows[0][0].size());
+        lag = (int)std::min<size_t>(std::max<size_t>(1, ((size_t)full_grid + per_row - 1) / per_row), 64);
+    }
+    hp.lag = lag < 0 ? 0 : lag;
+    const size_t L = (size_t)hp.lag;
+    bool has_phase1 = false;
+    for (auto& r : rows[1])
+        has_phase1 |= !r.empty();
+    const size_t L2 = has_phase1 ? 2 * L : L;
+    for (size_t t = 0; L > 0 && t < max_chunks + L2; ++t) {
+        if (t < max_chunks)
+            for (Deferred& d : rows[0][t])
+                b.emit(d.p, d.kind, d.op, d.ch);
+        if (t >= L && t - L < max_chunks)
+            for (Deferred& d : rows[1][t - L])
+                b.emit(d.p, d.kind, d.op, d.ch);
+        if (t >= L2 && t - L2 < max_chunks)
+            for (Deferred& d : rows[2][t - L2])
+                b.emit(d.p, d.kind, d.op, d.ch);
+    }
+
     if (hp.items.size() >= (1ull << 31) || hp.refs.size() >= (1ull << 32) || hp.syncs.size() >= (1ull << 32))
         return PL_ERR_UNSUPPORTED;
     hp.nflags = staged ? (uint32_t)((uint64_t)R * slots_per_rank) : next_flag;
+    hp.all_aligned = 1;
     for (const Item& it : hp.items) {
         if (it.nsrc > kMaxRanks || it.ndst > kMaxRanks || it.nsrc == 0 || it.ndst == 0)
             return PL_ERR_UNSUPPORTED;  // the kernel holds at most 64 sources and 64 destinations
         hp.ops |= it.op ? kOpsSum : kOpsCopy;
+        for (uint32_t k = it.ref; k < it.ref + it.nsrc + it.ndst; ++k) {
+            const Ref& f = hp.refs[k];
+            if ((f.offset * S) % 16 || (it.rows > 1 && (f.stride * S) % 16))
+                hp.all_aligned = 0;
+        }
     }
     if (tickets && !waits_precede(hp))
         return PL_ERR_NOMEM;
@@ -827,6 +892,23 @@ pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype d
     s.bytes_read = bytes_read;
     s.bytes_written = bytes_written;
     return PL_OK;
+}
+
+// The work list of a layout pair: the automatic lag is tried first; a lag the
+// ring cannot hold (a slot would be reused before its consumers) or that
+// breaks the claim-order rule falls back to smaller ones, down to none.
+pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                 const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, HostPlan& hp)
+{
+    pl_status st = derive_order(in, out, op, dt, R, pol, num_sms, ctas_per_sm, scratch_bytes, -1, hp);
+    if (st != PL_ERR_NOMEM)
+        return st;
+    for (int lag = hp.lag / 2; lag >= 0; lag = lag > 1 ? lag / 2 : lag - 1) {
+        st = derive_order(in, out, op, dt, R, pol, num_sms, ctas_per_sm, scratch_bytes, lag, hp);
+        if (st != PL_ERR_NOMEM)
+            return st;
+    }
+    return st;
 }
 
 }  // namespace
@@ -1279,6 +1361,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.dtype = dt;
     a.nbufs = 2 * R + 1;
     a.ops = dp->hp.ops;
+    a.all_aligned = dp->hp.all_aligned;
     a.epoch = ++ctx->epoch;
     a.timeout_ns = rp.timeout_ns;
     a.drop_notify = rp.drop_notify;
@@ -1354,6 +1437,7 @@ int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bu
     out.syncs = std::move(hp.syncs);
     out.nflags = hp.nflags;
     out.ops = hp.ops;
+    out.all_aligned = hp.all_aligned;
     out.ctas = hp.stats.ctas;
     out.uses_tickets = hp.stats.uses_tickets;
     return PL_OK;

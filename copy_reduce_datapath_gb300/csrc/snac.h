@@ -82,7 +82,7 @@ struct LaunchArgs {
     int32_t dtype;               // 0 bf16, 1 fp32
     int32_t nbufs;
     int32_t ops;                 // kOpsCopy | kOpsSum present in the list
-    int32_t pad0;
+    int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
     unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
     unsigned long long timeout_ns;
     long long drop_notify;       // item index whose notifies are skipped, or -1
@@ -105,6 +105,7 @@ struct HostWorkList {
     std::vector<Sync> syncs;
     uint32_t nflags = 0;
     int ops = 0;
+    int all_aligned = 0;
     int ctas = 1;
     int uses_tickets = 0;
 };
