@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--case", default=None, choices=sorted(CASES),
+                    help="time one collective of the other workloads instead of the step (prints its own line)")
+    ap.add_argument("--policy", default="", help="policy overrides for --case, e.g. path=2,chunk_bytes=262144")
     return ap.parse_args()
 
 
@@ -491,6 +494,121 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------------------ single cases
+
+CASES = {
+    # name: (collective, dtype, description)
+    "allgather": ("allgather", "bf16", "AllGather, R=8, bf16 N(0,1), equal partitions, T = output bytes per rank"),
+    "allreduce": ("allreduce", "bf16", "AllReduce, R=8, bf16 N(0,1), T = bytes per rank"),
+    "allreduce_r3_fp32": ("allreduce", "fp32", "AllReduce, R=3, fp32 integers in [-8, 8], T = bytes per rank"),
+    "reducescatter_bf16": ("reducescatter", "bf16", "ReduceScatter, R=8, bf16 U(-1,1), T = input bytes per rank"),
+    "reducescatter_fp32": ("reducescatter", "fp32", "ReduceScatter, R=8, fp32 U(-1,1), T = input bytes per rank"),
+    "reducescatter_inplace_bf16": ("reducescatter_inplace", "bf16", "ReduceScatter in place, R=8, bf16 U(-1,1)"),
+    "alltoall_moe": ("alltoall", "bf16", "AllToAll, R=8, per rank [4096 tokens, 7168] bf16, 8 token groups (T ignored)"),
+    "ulysses": ("ulysses", "bf16", "Ulysses AllToAll, R=8, per rank [16384, 32, 128] bf16, seq->head (T ignored)"),
+    "allgatherv": ("allgatherv", "bf16", "AllGatherV, R=8, bf16, Zipf s=0.125 lengths, T = output bytes per rank"),
+    "reducescatterv": ("reducescatterv", "bf16", "ReduceScatterV, R=8, bf16, Zipf s=0.125, T = input bytes per rank"),
+    "alltoallv": ("alltoallv", "bf16", "AllToAllV, R=8, bf16, Zipf s=0.125 rows, T = input bytes per rank"),
+}
+
+
+def run_case(args):
+    """Times `warmup` + `steps` launches of one workload; prints latency, algbw and HBM bandwidth."""
+    import torch
+    import synth
+    import __graft_entry__
+    __graft_entry__.build()
+    from copy_reduce_datapath_gb300 import purlin as P
+    kind, dt, desc = CASES[args.case]
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    S = 2 if dt == "bf16" else 4
+    pol = P.pl_policy_default()
+    for kv in filter(None, args.policy.split(",")):
+        k, v = kv.split("=")
+        setattr(pol, k, int(v))
+    Rr = 3 if args.case == "allreduce_r3_fp32" else R
+    ctx = P.pl_ctx_create(0, 1 << 30 if pol.path == P.PL_PATH_STAGED else 0)
+    T = args.T
+    N = T // S
+
+    def normal(seed, r, n):
+        return synth.device_normal_bf16(seed, r, n, dev) if dt == "bf16" else \
+            synth.device_uniform_pm1(seed, r, n, dev, tdt)
+
+    if kind == "allgather":
+        n = N // Rr
+        ins = [normal(1, r, n) for r in range(Rr)]
+        outs = [torch.empty(n * Rr, dtype=tdt, device=dev) for _ in range(Rr)]
+        lin, lout, op = P.pl_layout_rank_owned(Rr, [n] * Rr), P.pl_layout_partitioned(Rr, [n] * Rr), "copy"
+        moved = (n * Rr + Rr * n * Rr) * S
+    elif kind == "allreduce":
+        if dt == "fp32":
+            ins = [torch.from_numpy(synth.int_uniform_f32(0, r, N)).to(dev) for r in range(Rr)]
+        else:
+            ins = [normal(1, 100 + r, N) for r in range(Rr)]
+        outs = [torch.empty(N, dtype=tdt, device=dev) for _ in range(Rr)]
+        lin = lout = P.pl_layout_partitioned(Rr, synth.equal_lengths(N, Rr))
+        op, moved = "sum", 2 * Rr * N * S
+    elif kind in ("reducescatter", "reducescatter_inplace", "reducescatterv"):
+        lens = synth.zipf_lengths(N, Rr, 0.125, seed=4) if kind == "reducescatterv" else [N // Rr] * Rr
+        ins = [synth.device_uniform_pm1(2, r, N, dev, tdt) for r in range(Rr)]
+        lin = P.pl_layout_partitioned(Rr, lens)
+        if kind == "reducescatter_inplace":
+            outs, lout = ins, P.pl_layout_rank_owned_inplace(Rr, lens)
+        else:
+            outs = [torch.empty(lens[k], dtype=tdt, device=dev) for k in range(Rr)]
+            lout = P.pl_layout_rank_owned(Rr, lens)
+        op, moved = "sum", (Rr * N + N) * S
+    elif kind == "allgatherv":
+        lens = synth.zipf_lengths(N, Rr, 0.125, seed=4)
+        ins = [normal(4, r, lens[r]) for r in range(Rr)]
+        outs = [torch.empty(N, dtype=tdt, device=dev) for _ in range(Rr)]
+        lin, lout, op = P.pl_layout_rank_owned(Rr, lens), P.pl_layout_partitioned(Rr, lens), "copy"
+        moved = (N + Rr * N) * S
+    elif kind in ("alltoall", "alltoallv", "ulysses"):
+        if kind == "alltoall":
+            n = 4096 * 7168
+            m = [[n // Rr] * Rr for _ in range(Rr)]
+            lin, lout = P.pl_layout_alltoall_in(Rr, m), P.pl_layout_alltoall_out(Rr, m)
+        elif kind == "ulysses":
+            n = 16384 * 32 * 128
+            lin, lout = P.pl_layout_ulysses_in(Rr, 16384, 32, 128), P.pl_layout_ulysses_out(Rr, 16384, 32, 128)
+            m = [[n // Rr] * Rr for _ in range(Rr)]
+        else:
+            m = synth.zipf_matrix(N, Rr, 0.125, seed=4)
+            n = N
+            lin, lout = P.pl_layout_alltoall_in(Rr, m), P.pl_layout_alltoall_out(Rr, m)
+        ins = [normal(3, r, sum(m[r])) for r in range(Rr)]
+        outs = [torch.empty(sum(m[r][j] for r in range(Rr)), dtype=tdt, device=dev) for j in range(Rr)]
+        op, moved = "copy", 2 * Rr * n * S
+        T = n * S
+    stream = torch.cuda.current_stream()
+
+    def call():
+        P.pl_collective(ctx, lin, lout, op, dt, Rr, P.ptrs(ins), P.counts(ins), P.ptrs(outs), P.counts(outs), pol,
+                        stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert P.pl_ctx_status(ctx, stream.cuda_stream) == P.PL_OK
+    us = a.elapsed_time(b) * 1e3 / max(1, args.steps)
+    peak, kind_peak = measured_peaks()
+    print(json.dumps({"case": args.case, "workload": desc, "T_bytes": T, "policy": args.policy or "default",
+                      "steps": args.steps, "us": round(us, 2), "algbw_GBps": round(T / us / 1e3, 2),
+                      "hbm_GBps": round(moved / us / 1e3, 1), "frac_of_peak": round(moved / us / 1e3 / peak, 4),
+                      "peak_GBps": peak, "peak_kind": kind_peak}), flush=True)
+    P.pl_ctx_destroy(ctx)
+
+
 def run_reference(args):
     """The oracle on the host cores: the reference arm of this build (the pages
     ship no code).  Each timed step is a bounded sample of the workload; at most
@@ -527,7 +645,9 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

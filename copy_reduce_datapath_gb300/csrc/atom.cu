@@ -28,7 +28,8 @@ namespace purlin {
 namespace {
 
 constexpr int kStatusTimeout = 6;  // PL_ERR_TIMEOUT
-constexpr int kCtasPerSm = 1;
+constexpr int kCtasPerSm = 1;  // 512 threads with up to 128 registers each
+constexpr int kCopyUnroll = 8; // 16-byte vectors a thread keeps in flight in the copy bodies
 
 // ------------------------------------------------------- memory-model helpers
 
@@ -110,26 +111,29 @@ __device__ __forceinline__ unsigned long long tag(const LaunchArgs& a, unsigned 
     return (a.epoch << 24) | (unsigned long long)(use + 1u);
 }
 
-// Thread 0 of the CTA: every wait of the item.
-__device__ bool run_waits(const LaunchArgs& a, const Item& it)
+// Warp 0 of the CTA: every wait of the item, one flag per lane (lanes take
+// flags lane, lane + 32, ...), so an item's waits overlap instead of costing
+// one round trip each.  Returns, in every lane, whether all waits passed.
+__device__ bool run_waits(const LaunchArgs& a, const Item& it, int lane)
 {
-    if (ld_relaxed_s32(a.st.abort))
-        return false;
-    for (unsigned k = 0; k < it.nwait; ++k) {
+    bool ok = ld_relaxed_s32(a.st.abort) == 0;
+    for (unsigned k = (unsigned)lane; ok && k < it.nwait; k += 32) {
         const Sync s = a.syncs[it.sync + k];
         const unsigned long long* f = s.type == kWaitFull ? a.st.full + s.flag : a.st.done + s.flag;
-        if (!wait_at_least(f, tag(a, s.use), a))
-            return false;
+        ok = wait_at_least(f, tag(a, s.use), a);
     }
-    return true;
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// Thread 0 of the CTA, after a barrier that follows the item's stores.
-__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index)
+// Warp 0 of the CTA, after a barrier that follows the item's stores: the
+// notifies and credits of the item, one flag per lane.  Each posting lane
+// fences the CTA's writes (ordered before it by the barrier) ahead of its
+// release.
+__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index, int lane)
 {
-    __threadfence();
-    for (unsigned k = it.nwait; k < (unsigned)it.nwait + it.npost; ++k) {
-        const Sync s = a.syncs[it.sync + k];
+    for (unsigned k = (unsigned)lane; k < it.npost; k += 32) {
+        const Sync s = a.syncs[it.sync + it.nwait + k];
+        __threadfence();
         if (s.type == kNotify) {
             if ((long long)index == a.drop_notify)
                 continue;  // test hook: consumers of this item will time out
@@ -322,11 +326,10 @@ struct ItemShared {
 // Copy of nv 16-byte vectors from one source to every destination in `mask`.
 // The destinations are 16-byte aligned at `body`; the source is `q` bytes past
 // a 16-byte boundary (QALIGNED: q == 0).  U vectors in flight per thread.
-template <bool QALIGNED>
+template <bool QALIGNED, int U>
 __device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
                                        unsigned nv, int tid, int nthr)
 {
-    constexpr int U = QALIGNED ? 8 : 4;
     const char* src = SRC_ROW(sh, 0, row) + body;
     const int q = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
     const char* base = src - q;
@@ -370,46 +373,72 @@ __device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long lo
 
 // Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
 // to every destination in `mask`.  G sources in flight per thread.
-template <int S, bool QALIGNED>
-__device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                      size_t body, unsigned nv, int tid, int nthr)
+// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
+// to every destination in `mask`.  Aligned sources: U vectors x G sources
+// (U * G = 8 loads) in flight per thread, U chosen from the source count so
+// that few sources still keep the memory system busy.  Sources at mixed
+// misalignments (rare) are loaded one at a time and realigned.
+template <int S, int U>
+__device__ __forceinline__ void sum_aligned(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                            size_t body, unsigned nv, int tid, int nthr)
 {
-    constexpr int G = QALIGNED ? 8 : 1;
-    for (unsigned v = tid; v < nv; v += nthr) {
-        Acc<S> acc;
+    constexpr int G = 8 / U;
+    const unsigned step = (unsigned)nthr * U;
+    for (unsigned v0 = tid; v0 < nv; v0 += step) {
+        Acc<S> acc[U];
         for (int s0 = 0; s0 < nsrc; s0 += G) {
-            uint4 x[G];
-            if constexpr (QALIGNED) {
+            uint4 x[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
 #pragma unroll
                 for (int g = 0; g < G; ++g)
-                    if (s0 + g < nsrc)
-                        x[g] = ld16(SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16);
-            } else {
-                uint4 lo[G], hi[G];
-                int q[G];
+                    if (s0 + g < nsrc && v < nv)
+                        x[u][g] = ld16(SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     if (s0 + g < nsrc) {
-                        const char* p = SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16;
-                        q[g] = (int)(reinterpret_cast<uintptr_t>(p) & 15u);
-                        lo[g] = ld16(p - q[g]);
-                        hi[g] = q[g] ? ld16(p - q[g] + 16) : lo[g];
+                        if (s0 + g == 0)
+                            acc[u].set(x[u][g]);
+                        else
+                            acc[u].add(x[u][g]);
                     }
                 }
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if (s0 + g < nsrc)
-                        x[g] = q[g] ? realign(lo[g], hi[g], q[g]) : lo[g];
             }
+        }
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                if (s0 + g < nsrc) {
-                    if (s0 + g == 0)
-                        acc.set(x[g]);
-                    else
-                        acc.add(x[g]);
+        for (int u = 0; u < U; ++u) {
+            const unsigned v = v0 + u * nthr;
+            if (v < nv) {
+                const uint4 out = acc[u].pack();
+#pragma unroll 1
+                for (unsigned long long m = mask; m; m &= m - 1) {
+                    const int d = __ffsll((long long)m) - 1;
+                    st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, out);
                 }
             }
+        }
+    }
+}
+
+template <int S>
+__device__ __forceinline__ void sum_mixed(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                          size_t body, unsigned nv, int tid, int nthr)
+{
+    for (unsigned v = tid; v < nv; v += nthr) {
+        Acc<S> acc;
+        for (int s = 0; s < nsrc; ++s) {
+            const char* p = SRC_ROW(sh, s, row) + body + (size_t)v * 16;
+            const int q = (int)(reinterpret_cast<uintptr_t>(p) & 15u);
+            const uint4 lo = ld16(p - q);
+            const uint4 x = q ? realign(lo, ld16(p - q + 16), q) : lo;
+            if (s == 0)
+                acc.set(x);
+            else
+                acc.add(x);
         }
         const uint4 out = acc.pack();
 #pragma unroll 1
@@ -418,6 +447,15 @@ __device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigne
             st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, out);
         }
     }
+}
+
+template <int S, bool WIDE>
+__device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                         size_t body, unsigned nv, int tid, int nthr)
+{
+    // 8 loads in flight per thread either way: 1 vector x 8 sources when every
+    // sum has 8 or more sources, else 2 vectors x 4 sources.
+    sum_aligned<S, WIDE ? 1 : 2>(sh, nsrc, mask, row, body, nv, tid, nthr);
 }
 
 // Thread 0: copies `nbytes` (a multiple of 16, both ends 16-byte aligned)
@@ -557,13 +595,12 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
 // addresses in every source and destination: one flat index over
 // rows x vectors-per-row spread over the whole CTA (no per-row heads, tails
 // or realignment).
-template <int S, bool SUM>
+template <int S, bool SUM, int U>
 __device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int ndst, unsigned rows, unsigned vpr,
                                             int tid, int nthr)
 {
     const unsigned total = rows * vpr;
     if constexpr (!SUM) {
-        constexpr int U = 8;
         for (unsigned v0 = tid; v0 < total; v0 += (unsigned)nthr * U) {
             uint4 x[U];
             unsigned rr[U], cc[U];
@@ -672,16 +709,16 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
             if (tid == 0)
                 bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
         } else if (ALIGN || aligned)
-            copy_body<true>(sh, mask, row, body, nv, tid, nthr);
+            copy_body<true, kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
         else
             shifted_body<S, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
     } else if (OPS & kOpsSum) {
         if (ALIGN || aligned)
-            sum_body<S, true>(sh, nsrc, mask, row, body, nv, tid, nthr);
+            sum_body<S, (OPS & kOpsWide) != 0>(sh, nsrc, mask, row, body, nv, tid, nthr);
         else if (uniform)
             shifted_body<S, true>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
         else
-            sum_body<S, false>(sh, nsrc, mask, row, body, nv, tid, nthr);
+            sum_mixed<S>(sh, nsrc, mask, row, body, nv, tid, nthr);
     }
 }
 
@@ -702,9 +739,10 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
         if (flat) {
             const unsigned vpr = (unsigned)(cols * S / 16);
             if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1))
-                flat2d_body<S, false>(sh, 1, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
+                flat2d_body<S, false, kCopyUnroll>(sh, 1, ndst, rows, vpr, (int)threadIdx.x,
+                                                                     (int)blockDim.x);
             else if (OPS & kOpsSum)
-                flat2d_body<S, true>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
+                flat2d_body<S, true, 1>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
             return;
         }
     }
@@ -815,13 +853,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid
             nref = a.refs[nit.ref + tid];
         unsigned i2 = ~0u;
         Item h2{};
-        if (tid == 0) {
-            if (next_index < a.nitems) {
-                i2 = claim(a, k + 2);
-                if (i2 < a.nitems)
-                    h2 = a.items[i2];
-            }
-            s_ok = it.nwait ? run_waits(a, it) : 1;
+        if (tid == 0 && next_index < a.nitems) {
+            i2 = claim(a, k + 2);
+            if (i2 < a.nitems)
+                h2 = a.items[i2];
+        }
+        if (tid < 32) {
+            const bool ok = it.nwait ? run_waits(a, it, tid) : true;
+            if (tid == 0)
+                s_ok = ok ? 1 : 0;
         }
         __syncthreads();
         if (s_ok)
@@ -834,8 +874,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid
             slot[cur].item = h2;
         }
         __syncthreads();
-        if (tid == 0 && s_ok && it.npost)
-            run_posts(a, it, index);
+        if (tid < 32 && s_ok && it.npost)
+            run_posts(a, it, index, tid);
     }
 
     if (a.use_tickets && tid == 0) {
@@ -879,6 +919,8 @@ cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_
         return launch_one<S, kOpsCopy, BULK, ALIGN>(args, ctas, stages, stream);
     if (args.ops == kOpsSum)
         return launch_one<S, kOpsSum, false, ALIGN>(args, ctas, stages, stream);
+    if (args.ops == (kOpsSum | kOpsWide))
+        return launch_one<S, kOpsSum | kOpsWide, false, ALIGN>(args, ctas, stages, stream);
     return launch_one<S, kOpsCopy | kOpsSum, BULK, ALIGN>(args, ctas, stages, stream);
 }
 

@@ -35,6 +35,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr uint64_t kMinChunkBytes = 8 << 10;
 constexpr uint64_t kMaxChunkBytes = 4 << 20;
 constexpr uint64_t kTicketedChunkBytes = 256 << 10;
+constexpr uint64_t kBulkAutoBytes = 64ull << 20;  // automatic bulk-ring datapath from this many bytes moved
 constexpr int kItemsPerCta = 4;       // auto chunking aims at this many items per CTA
 constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threads x 128 registers)
 constexpr size_t kMaxCachedPlans = 1024;
@@ -306,6 +307,8 @@ struct ResolvedPolicy {
     int path;       // PL_PATH_ZS / PL_PATH_STAGED
     int ar_form;    // PL_AR_FUSED / PL_AR_COMPOSED
     int datapath;   // PL_ATOM_VECTOR / PL_ATOM_BULK
+    bool datapath_auto;
+    bool stages_auto;
     int ctas;       // 0 = auto
     int stages;
     uint64_t chunk_bytes;
@@ -330,6 +333,8 @@ pl_status resolve_policy(const pl_policy* p, ResolvedPolicy& rp)
     rp.path = p->path == PL_PATH_AUTO ? PL_PATH_ZS : p->path;
     rp.ar_form = p->allreduce_form == PL_AR_AUTO ? PL_AR_FUSED : p->allreduce_form;
     rp.datapath = p->datapath == PL_ATOM_AUTO ? PL_ATOM_VECTOR : p->datapath;
+    rp.datapath_auto = p->datapath == PL_ATOM_AUTO;
+    rp.stages_auto = p->stages == 0;
     rp.ctas = p->ctas;
     rp.stages = p->stages ? p->stages : 4;
     // Work items address columns with 32-bit counts: keep chunks well below 2^32 elements.
@@ -829,11 +834,13 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
 
     // Emit: producers of row t, their consumers L rows later, gathers of
     // reduced chunks one more lag later (or L when nothing sits between).
-    // The automatic lag puts about one grid of items between a producer and
+    // The automatic lag puts about two grids of items between a producer and
     // its first consumer, so consumers are claimed once producers are done.
     if (lag < 0 && max_chunks > 0) {
         size_t per_row = std::max<size_t>(1, rows[0][0].size());
-        lag = (int)std::min<size_t>(std::max<size_t>(1, ((size_t)full_grid + per_row - 1) / per_row), 64);
+        // each CTA holds up to two claimed items, so about two grids of items
+        // may be claimed but not yet finished
+        lag = (int)std::min<size_t>(((size_t)2 * full_grid + per_row - 1) / per_row + 1, 64);
     }
     hp.lag = lag < 0 ? 0 : lag;
     const size_t L = (size_t)hp.lag;
@@ -857,7 +864,10 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         return PL_ERR_UNSUPPORTED;
     hp.nflags = staged ? (uint32_t)((uint64_t)R * slots_per_rank) : next_flag;
     hp.all_aligned = 1;
+    bool wide = true;
     for (const Item& it : hp.items) {
+        if (it.op)
+            wide &= it.nsrc >= 8;
         if (it.nsrc > kMaxRanks || it.ndst > kMaxRanks || it.nsrc == 0 || it.ndst == 0)
             return PL_ERR_UNSUPPORTED;  // the kernel holds at most 64 sources and 64 destinations
         hp.ops |= it.op ? kOpsSum : kOpsCopy;
@@ -867,6 +877,10 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                 hp.all_aligned = 0;
         }
     }
+    // bf16 sums of 8+ sources stream best as 1 vector x 8 sources per step;
+    // fp32 sums and fewer sources as 2 vectors x 4 sources (measured on GB300).
+    if (hp.ops == kOpsSum && wide && dt == PL_BF16)
+        hp.ops |= kOpsWide;
     if (tickets && !waits_precede(hp))
         return PL_ERR_NOMEM;
 
@@ -1371,8 +1385,19 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         a.bufs[R + r] = (char*)out_bufs[r];
     }
     a.bufs[2 * R] = ctx->scratch;
+    // Codesign policy for the datapath: large copy-only plans over 16-byte
+    // aligned regions stream through the bulk-copy ring (one shared-memory
+    // read per chunk, one bulk store per destination); everything else uses
+    // the vector datapath.
     bool bulk = rp.datapath == PL_ATOM_BULK;
-    cudaError_t e = launch_snac(a, ps.ctas, bulk, rp.stages, (cudaStream_t)stream);
+    int stages = rp.stages;
+    if (rp.datapath_auto && dp->hp.ops == kOpsCopy && dp->hp.all_aligned &&
+        ps.bytes_read + ps.bytes_written >= kBulkAutoBytes) {
+        bulk = true;
+        if (rp.stages_auto)
+            stages = kBulkMaxStages;
+    }
+    cudaError_t e = launch_snac(a, ps.ctas, bulk, stages, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(ctx, e);
     ++ctx->launches;

@@ -22,6 +22,7 @@ enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3
 // a copy-only or sum-only list gets code without the other path.
 constexpr int kOpsCopy = 1;
 constexpr int kOpsSum = 2;
+constexpr int kOpsWide = 4;  // every sum has at least 8 sources: one vector x 8 sources per step
 
 // One work item: move a rows x cols block from nsrc sources (copy if nsrc == 1,
 // rank-ordered fp32 sum otherwise) into ndst destinations.  Refs

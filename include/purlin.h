@@ -102,7 +102,8 @@ typedef struct pl_policy {
 #define PL_AR_FUSED     1 /* one work item reduces a chunk and writes it to every output of its name */
 #define PL_AR_COMPOSED  2 /* Figure 6: the owner reduces its partition's chunk, notifies, the others gather it */
 
-#define PL_ATOM_AUTO    0 /* vector */
+#define PL_ATOM_AUTO    0 /* bulk ring (8 stages) for copy-only plans over 16-byte aligned regions moving >= 64 MiB,
+                             vector otherwise */
 #define PL_ATOM_VECTOR  1 /* 16-byte vector loads and stores by every thread */
 #define PL_ATOM_BULK    2 /* cp.async.bulk through a shared-memory ring (COPY work items; others use vector) */
 
