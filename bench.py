@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--case", default=None, choices=sorted(CASES),
                     help="time one collective of the other workloads instead of the step (prints its own line)")
     ap.add_argument("--policy", default="", help="policy overrides for --case, e.g. path=2,chunk_bytes=262144")
+    ap.add_argument("--depth-sweep", action="store_true",
+                    help="Atom copy of 256 MiB: bandwidth vs CTA count and bulk-ring depth (prints its own line)")
+    ap.add_argument("--copy-engine", action="store_true",
+                    help="AllGather by one device-to-device memcpy per (source, destination) pair, beside the kernel")
     return ap.parse_args()
 
 
@@ -609,6 +613,102 @@ def run_case(args):
     P.pl_ctx_destroy(ctx)
 
 
+def run_depth_sweep(args):
+    """One 256 MiB copy (one source region to one destination region) through the
+    Atom datapath: the vector path and the cp.async.bulk ring at depths 1..8,
+    each at several CTA counts.  Reports read + write bandwidth."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from copy_reduce_datapath_gb300 import purlin as P
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    n = (256 << 20) // 2
+    src = torch.randn(n, device=dev).to(torch.bfloat16)
+    dst = torch.empty_like(src)
+    ctx = P.pl_ctx_create(0, 0)
+    L = P.pl_layout_rank_owned(1, [n])
+    stream = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak, peak_kind = measured_peaks()
+    rows = []
+    for ctas in (8, 16, 32, 64, sms):
+        for datapath, stages in [(P.PL_ATOM_VECTOR, 0)] + [(P.PL_ATOM_BULK, d) for d in range(1, 9)]:
+            pol = P.pl_policy_default(datapath=datapath, stages=stages, ctas=ctas)
+
+            def call():
+                P.pl_collective(ctx, L, L, "copy", "bf16", 1, [src.data_ptr()], [n], [dst.data_ptr()], [n], pol,
+                                stream.cuda_stream)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(10):
+                call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / 10
+            rows.append({"ctas": ctas, "datapath": "vector" if datapath == P.PL_ATOM_VECTOR else "bulk",
+                         "stages": stages, "us": round(us, 1), "GBps": round(2 * n * 2 / us / 1e3, 1)})
+    assert P.pl_ctx_status(ctx, stream.cuda_stream) == P.PL_OK
+    torch.testing.assert_close(dst, src, rtol=0, atol=0)
+    print(json.dumps({"sweep": "atom_copy_256MiB", "bytes_moved": 2 * n * 2, "peak_GBps": peak,
+                      "peak_kind": peak_kind, "rows": rows}), flush=True)
+    P.pl_ctx_destroy(ctx)
+
+
+def run_copy_engine(args):
+    """AllGather (R=8, bf16, T bytes of output per rank) done by one contiguous
+    device-to-device copy per (source, destination) pair -- the copy-engine
+    route that launches no kernel -- timed beside the library's AllGather."""
+    import torch
+    import synth
+    import __graft_entry__
+    __graft_entry__.build()
+    from copy_reduce_datapath_gb300 import purlin as P
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    T = args.T
+    n = T // 2 // R
+    ins = [synth.device_normal_bf16(SEED, r, n, dev) for r in range(R)]
+    outs = [torch.empty(n * R, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    stream = torch.cuda.current_stream()
+
+    def by_memcpy():
+        for r in range(R):
+            for j in range(R):
+                outs[r][j * n:(j + 1) * n].copy_(ins[j], non_blocking=True)
+
+    ctx = P.pl_ctx_create(0, 0)
+    lin, lout = P.pl_layout_rank_owned(R, [n] * R), P.pl_layout_partitioned(R, [n] * R)
+
+    def by_kernel():
+        P.pl_collective(ctx, lin, lout, "copy", "bf16", R, P.ptrs(ins), P.counts(ins), P.ptrs(outs), P.counts(outs),
+                        None, stream.cuda_stream)
+
+    res = {}
+    for name, fn in (("memcpy_per_pair", by_memcpy), ("snac_kernel", by_kernel)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(max(1, args.steps)):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / max(1, args.steps)
+        res[name] = {"us": round(us, 2), "algbw_GBps": round(T / us / 1e3, 2),
+                     "hbm_GBps": round((n * R + R * n * R) * 2 / us / 1e3, 1)}
+        for r in range(R):
+            for j in (0, R - 1):
+                assert torch.equal(outs[r][j * n:(j + 1) * n], ins[j])
+    print(json.dumps({"compare": "allgather_copy_engine_vs_kernel", "R": R, "T_bytes": T, "results": res}),
+          flush=True)
+    P.pl_ctx_destroy(ctx)
+
+
 def run_reference(args):
     """The oracle on the host cores: the reference arm of this build (the pages
     ship no code).  Each timed step is a bounded sample of the workload; at most
@@ -645,7 +745,11 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.case:
+    if args.depth_sweep:
+        run_depth_sweep(args)
+    elif args.copy_engine:
+        run_copy_engine(args)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -52,6 +52,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if verbose else []
+    # Developer knob for experiments with alternative builds (e.g. -DPL_STORE_STREAMING).
+    extra += os.environ.get("PURLIN_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, src + ".o")

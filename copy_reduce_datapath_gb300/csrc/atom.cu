@@ -74,7 +74,12 @@ __device__ __forceinline__ unsigned long long global_ns()
 // Streaming 16-byte load that is served from L2 (data may have been written
 // by another CTA of this launch after a flag acquire).
 __device__ __forceinline__ uint4 ld16(const char* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+#if defined(PL_STORE_STREAMING)
+// Developer build option: evict-first stores for outputs nobody rereads.
+__device__ __forceinline__ void st16(char* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+#else
 __device__ __forceinline__ void st16(char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+#endif
 
 // ------------------------------------------------------------- bounded waits
 
