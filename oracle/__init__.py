@@ -7,8 +7,9 @@ and its ``libpurlin1``) shares no code with it and never imports it.
 The arithmetic lives in ``oracle.c`` (plain C loops, one element at a time);
 this module only marshals numpy arrays into it.  Element storage:
 
-* ``"bf16"`` arrays are ``numpy.uint16`` bit patterns;
-* ``"fp32"`` arrays are ``numpy.float32``.
+* ``"bf16"`` and ``"fp16"`` arrays are ``numpy.uint16`` bit patterns;
+* ``"fp32"`` arrays are ``numpy.float32``;
+* ``"fp8"`` arrays are ``numpy.uint8`` bytes (any 1-byte format: moved, never reduced).
 
 Every function cites the passage of "Purlin: Separating Orchestration from the
 Datapath of Collectives" that it writes out:
@@ -21,6 +22,7 @@ Datapath of Collectives" that it writes out:
 ``ulysses_a2a``           Table 2, Ulysses row (sequence <-> head)
 ``collective``            abstract: input layout + output layout + op
 ``f32_to_bf16``           the output rounding (IEEE round-to-nearest-even)
+``f32_to_f16``            the same rounding to IEEE binary16
 ========================  ==============================================
 
 Parity pins live in ``tests/test_oracle_pins.py``; every function above is
@@ -37,9 +39,10 @@ import numpy as np
 
 from . import build as _build
 
-BF16, FP32 = 0, 1
-COPY, SUM = 0, 1
-_DT = {"bf16": (BF16, np.uint16), "fp32": (FP32, np.float32)}
+BF16, FP32, FP16, FP8 = 0, 1, 2, 3
+COPY, SUM, MAX = 0, 1, 2
+_DT = {"bf16": (BF16, np.uint16), "fp32": (FP32, np.float32), "fp16": (FP16, np.uint16), "fp8": (FP8, np.uint8)}
+_OPS = {"copy": COPY, "sum": SUM, "max": MAX}
 
 
 class _Part(C.Structure):
@@ -77,6 +80,16 @@ def _inputs(ins, dtype):
     return code, npdt, out
 
 
+def _reducible(dtype):
+    if dtype == "fp8":
+        raise ValueError("1-byte (fp8) elements are only moved, never reduced")
+
+
+def f16_to_f32(h) -> np.ndarray:
+    """IEEE binary16 bit patterns -> fp32 values (numpy's float16 view; exact)."""
+    return np.ascontiguousarray(h, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
 def bf16_to_f32(h) -> np.ndarray:
     """bf16 bit patterns -> fp32 values (exact: a bf16 is the top half of an fp32)."""
     h = np.ascontiguousarray(h, dtype=np.uint16)
@@ -93,6 +106,12 @@ class Oracle:
         vp, u64p = C.c_void_p, C.POINTER(C.c_uint64)
         L.orc_f32_to_bf16_n.argtypes = [C.c_void_p, C.c_void_p, C.c_uint64]
         L.orc_f32_to_bf16_n.restype = None
+        L.orc_f32_to_f16_n.argtypes = [C.c_void_p, C.c_void_p, C.c_uint64]
+        L.orc_f32_to_f16_n.restype = None
+        L.orc_reducescatter_op.argtypes = [C.c_int, C.c_int, C.c_int, C.POINTER(vp), u64p, C.POINTER(vp)]
+        L.orc_reducescatter_op.restype = None
+        L.orc_allreduce_op.argtypes = [C.c_int, C.c_int, C.c_int, C.POINTER(vp), C.c_uint64, C.POINTER(vp)]
+        L.orc_allreduce_op.restype = None
         for name in ("orc_allgather", "orc_reducescatter", "orc_alltoall"):
             getattr(L, name).argtypes = [C.c_int, C.c_int, C.POINTER(vp), u64p, C.POINTER(vp)]
             getattr(L, name).restype = None
@@ -118,6 +137,14 @@ class Oracle:
             self.lib.orc_f32_to_bf16_n(x.ctypes.data, y.ctypes.data, x.size)
         return y
 
+    def f32_to_f16(self, x) -> np.ndarray:
+        """fp32 values -> IEEE binary16 bit patterns, round-to-nearest-even."""
+        x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+        y = np.empty(x.size, dtype=np.uint16)
+        if x.size:
+            self.lib.orc_f32_to_f16_n(x.ctypes.data, y.ctypes.data, x.size)
+        return y
+
     # ---------------------------------------------------------- collectives
 
     def allgather(self, ins, dtype: str):
@@ -129,26 +156,34 @@ class Oracle:
         self.lib.orc_allgather(R, code, _ptrs(ins), _u64(n), _ptrs(outs))
         return outs
 
-    def reducescatter(self, ins, lens, dtype: str):
-        """ReduceScatter(V): rank k receives the rank-ordered sum of partition k (Figure 4)."""
+    def reducescatter(self, ins, lens, dtype: str, op: str = "sum"):
+        """ReduceScatter(V): rank k receives the rank-ordered sum (or max) of partition k (Figure 4)."""
         code, npdt, ins = _inputs(ins, dtype)
+        _reducible(dtype)
         R = len(ins)
         lens = [int(x) for x in lens]
         if len(lens) != R or any(a.size != sum(lens) for a in ins):
             raise ValueError("reducescatter: each input must hold sum(lens) elements, R = len(lens)")
         outs = [np.empty(lens[k], dtype=npdt) for k in range(R)]
-        self.lib.orc_reducescatter(R, code, _ptrs(ins), _u64(lens), _ptrs(outs))
+        if op == "sum":
+            self.lib.orc_reducescatter(R, code, _ptrs(ins), _u64(lens), _ptrs(outs))
+        else:
+            self.lib.orc_reducescatter_op(R, code, _OPS[op], _ptrs(ins), _u64(lens), _ptrs(outs))
         return outs
 
-    def allreduce(self, ins, dtype: str):
-        """AllReduce: every rank receives the rank-ordered elementwise sum (direct definition)."""
+    def allreduce(self, ins, dtype: str, op: str = "sum"):
+        """AllReduce: every rank receives the rank-ordered elementwise sum (or max) (direct definition)."""
         code, npdt, ins = _inputs(ins, dtype)
+        _reducible(dtype)
         R = len(ins)
         count = ins[0].size
         if any(a.size != count for a in ins):
             raise ValueError("allreduce: inputs must have equal sizes")
         outs = [np.empty(count, dtype=npdt) for _ in range(R)]
-        self.lib.orc_allreduce(R, code, _ptrs(ins), count, _ptrs(outs))
+        if op == "sum":
+            self.lib.orc_allreduce(R, code, _ptrs(ins), count, _ptrs(outs))
+        else:
+            self.lib.orc_allreduce_op(R, code, _OPS[op], _ptrs(ins), count, _ptrs(outs))
         return outs
 
     def alltoall(self, ins, lens_matrix, dtype: str):
@@ -190,7 +225,7 @@ class Oracle:
         """
         code, npdt, ins = _inputs(ins, dtype)
         R = len(ins)
-        opc = {"copy": COPY, "sum": SUM}[op]
+        opc = _OPS[op]
 
         def flat(layout):
             if len(layout) != R:
@@ -230,16 +265,20 @@ def f32_to_bf16(x):
     return default().f32_to_bf16(x)
 
 
+def f32_to_f16(x):
+    return default().f32_to_f16(x)
+
+
 def allgather(ins, dtype):
     return default().allgather(ins, dtype)
 
 
-def reducescatter(ins, lens, dtype):
-    return default().reducescatter(ins, lens, dtype)
+def reducescatter(ins, lens, dtype, op="sum"):
+    return default().reducescatter(ins, lens, dtype, op)
 
 
-def allreduce(ins, dtype):
-    return default().allreduce(ins, dtype)
+def allreduce(ins, dtype, op="sum"):
+    return default().allreduce(ins, dtype, op)
 
 
 def alltoall(ins, lens_matrix, dtype):

@@ -22,6 +22,11 @@
  *     every add and no flush of subnormals, then rounded ONCE to the output type;
  *   - the composed AllReduce's intermediate y_k is that once-rounded value, so
  *     AllReduce equals the direct per-element definition bit for bit.
+ *   - the maximum is a rank-ordered fold that takes rank r's value when it is
+ *     greater (IEEE comparison), so NaN counts only from rank 0 and of two
+ *     zeros the earlier rank's sign is kept;
+ *   - fp16 follows the same fp32-accumulate, round-once rule as bf16; 1-byte
+ *     (fp8) elements are only moved, never reduced.
  *
  * Everything here is a plain loop over elements; nothing is blocked, fused or
  * reordered.  Build: plain C11, -O2 -fno-fast-math -ffp-contract=off.
@@ -35,8 +40,8 @@
 #error "the oracle needs fp32 arithmetic evaluated in fp32 (FLT_EVAL_METHOD == 0)"
 #endif
 
-enum { ORC_BF16 = 0, ORC_FP32 = 1 };
-enum { ORC_COPY = 0, ORC_SUM = 1 };
+enum { ORC_BF16 = 0, ORC_FP32 = 1, ORC_FP16 = 2, ORC_U8 = 3 };
+enum { ORC_COPY = 0, ORC_SUM = 1, ORC_MAX = 2 };
 
 /* ---------------------------------------------------------------- bf16 --- */
 
@@ -99,14 +104,94 @@ void orc_f32_to_bf16_n(const float* x, uint16_t* y, uint64_t n)
         y[i] = orc_f32_to_bf16(x[i]);
 }
 
+/* ---------------------------------------------------------------- fp16 --- */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+float orc_f16_to_f32(uint16_t h)
+{
+    int e = (h >> 10) & 0x1F, f = h & 0x3FF;
+    double v;
+    if (e == 31)
+        v = f ? (double)NAN : (double)INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -24);
+    else
+        v = ldexp(1.0 + f / 1024.0, e - 15);
+    return (float)((h & 0x8000) ? -v : v); /* every binary16 value is exact in fp32 */
+}
+
+/* fp32 -> binary16, round to nearest, ties to even, from the definition: on
+ * the binary16 grid of |x|'s binade (spacing 2^(e-10) for |x| in [2^e,
+ * 2^(e+1)), 2^-24 below 2^-14) take the nearer neighbour, the even multiple
+ * on a tie; a result of 2^16 or more is infinity.  All steps are exact in
+ * double precision (power-of-two scalings of an fp32 value). */
+uint16_t orc_f32_to_f16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7E00u);
+    if (isinf(x))
+        return (uint16_t)(sign | 0x7C00u);
+    const double a = fabs((double)x);
+    double ulp;
+    if (a < ldexp(1.0, -14)) {
+        ulp = ldexp(1.0, -24);
+    } else {
+        int e;
+        frexp(a, &e); /* a = m * 2^e, m in [0.5, 1): the binade is [2^(e-1), 2^e) */
+        ulp = ldexp(1.0, (e - 1) - 10);
+    }
+    const double q = a / ulp;
+    const double t = floor(q);
+    const double rem = q - t;
+    double n;
+    if (rem < 0.5)
+        n = t;
+    else if (rem > 0.5)
+        n = t + 1.0;
+    else
+        n = fmod(t, 2.0) == 0.0 ? t : t + 1.0;
+    const double v = n * ulp;
+    if (v >= 65536.0)
+        return (uint16_t)(sign | 0x7C00u);
+    if (v < ldexp(1.0, -14))
+        return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, -24)));
+    int e;
+    const double m = frexp(v, &e);
+    const int biased = (e - 1) + 15;
+    const uint16_t frac = (uint16_t)((m * 2.0 - 1.0) * 1024.0);
+    return (uint16_t)(sign | (uint16_t)(biased << 10) | frac);
+}
+
+void orc_f32_to_f16_n(const float* x, uint16_t* y, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; ++i)
+        y[i] = orc_f32_to_f16(x[i]);
+}
+
 /* ------------------------------------------------------- element access --- */
 
-static size_t esize(int dtype) { return dtype == ORC_BF16 ? 2u : 4u; }
+static size_t esize(int dtype)
+{
+    switch (dtype) {
+    case ORC_BF16:
+    case ORC_FP16:
+        return 2u;
+    case ORC_U8:
+        return 1u;
+    default:
+        return 4u;
+    }
+}
 
 static float load_f32(const void* buf, int dtype, uint64_t i)
 {
     if (dtype == ORC_BF16)
         return orc_bf16_to_f32(((const uint16_t*)buf)[i]);
+    if (dtype == ORC_FP16)
+        return orc_f16_to_f32(((const uint16_t*)buf)[i]);
     return ((const float*)buf)[i];
 }
 
@@ -114,6 +199,8 @@ static void store_f32(void* buf, int dtype, uint64_t i, float v)
 {
     if (dtype == ORC_BF16)
         ((uint16_t*)buf)[i] = orc_f32_to_bf16(v);
+    else if (dtype == ORC_FP16)
+        ((uint16_t*)buf)[i] = orc_f32_to_f16(v);
     else
         ((float*)buf)[i] = v;
 }
@@ -133,6 +220,26 @@ static float fold_ranks(int R, int dtype, const void* const* bufs, const uint64_
     return acc;
 }
 
+/* The maximum of one element position over R inputs, in rank order: start
+ * from rank 0's value and take rank r's value when it is greater.  NaN never
+ * compares greater, so a NaN counts only from rank 0, and of +0 and -0 the
+ * earlier rank's is kept. */
+static float fold_max(int R, int dtype, const void* const* bufs, const uint64_t* idx)
+{
+    float acc = load_f32(bufs[0], dtype, idx[0]);
+    for (int r = 1; r < R; ++r) {
+        const float v = load_f32(bufs[r], dtype, idx[r]);
+        if (v > acc)
+            acc = v;
+    }
+    return acc;
+}
+
+static float fold_op(int op, int R, int dtype, const void* const* bufs, const uint64_t* idx)
+{
+    return op == ORC_MAX ? fold_max(R, dtype, bufs, idx) : fold_ranks(R, dtype, bufs, idx);
+}
+
 /* ------------------------------------------------ the seven collectives --- */
 
 /* AllGather(V): rank j contributes n[j] elements; every rank r receives them
@@ -149,9 +256,10 @@ void orc_allgather(int R, int dtype, const void* const* in, const uint64_t* n, v
     }
 }
 
-/* ReduceScatter(V): every input is split into partitions of lengths n[0..R-1]
- * at prefix offsets o_k; rank k receives y_k[i] = round(sum_r in_r[o_k + i]). */
-void orc_reducescatter(int R, int dtype, const void* const* in, const uint64_t* n, void* const* out)
+/* ReduceScatter(V) with the reduction `op` (sum or max): every input is split
+ * into partitions of lengths n[0..R-1] at prefix offsets o_k; rank k receives
+ * y_k[i] = round(fold_r in_r[o_k + i]). */
+void orc_reducescatter_op(int R, int dtype, int op, const void* const* in, const uint64_t* n, void* const* out)
 {
     uint64_t idx[64];
     uint64_t o = 0;
@@ -159,23 +267,36 @@ void orc_reducescatter(int R, int dtype, const void* const* in, const uint64_t* 
         for (uint64_t i = 0; i < n[k]; ++i) {
             for (int r = 0; r < R; ++r)
                 idx[r] = o + i;
-            store_f32(out[k], dtype, i, fold_ranks(R, dtype, in, idx));
+            store_f32(out[k], dtype, i, fold_op(op, R, dtype, in, idx));
         }
         o += n[k];
     }
 }
 
-/* AllReduce, direct definition: out_r[i] = round(sum_r' in_r'[i]) for all r. */
-void orc_allreduce(int R, int dtype, const void* const* in, uint64_t count, void* const* out)
+/* ReduceScatter(V) with the sum (Figure 4). */
+void orc_reducescatter(int R, int dtype, const void* const* in, const uint64_t* n, void* const* out)
+{
+    orc_reducescatter_op(R, dtype, ORC_SUM, in, n, out);
+}
+
+/* AllReduce with the reduction `op`, direct definition: out_r[i] =
+ * round(fold_r' in_r'[i]) for all r. */
+void orc_allreduce_op(int R, int dtype, int op, const void* const* in, uint64_t count, void* const* out)
 {
     uint64_t idx[64];
     for (uint64_t i = 0; i < count; ++i) {
         for (int r = 0; r < R; ++r)
             idx[r] = i;
-        float s = fold_ranks(R, dtype, in, idx);
+        const float v = fold_op(op, R, dtype, in, idx);
         for (int r = 0; r < R; ++r)
-            store_f32(out[r], dtype, i, s);
+            store_f32(out[r], dtype, i, v);
     }
+}
+
+/* AllReduce with the sum. */
+void orc_allreduce(int R, int dtype, const void* const* in, uint64_t count, void* const* out)
+{
+    orc_allreduce_op(R, dtype, ORC_SUM, in, count, out);
 }
 
 /* AllToAll(V): source r splits its input into partitions of lengths
@@ -263,6 +384,8 @@ int orc_collective(int R, int op, int dtype,
                         src_rank[ns] = r;
                         ++ns;
                     }
+            if (op != ORC_COPY && dtype == ORC_U8)
+                return 1; /* 1-byte elements are moved, never reduced */
             if (op == ORC_COPY) {
                 if (ns != 1 || region_count(src[0]) != cnt)
                     return 1;
@@ -280,7 +403,7 @@ int orc_collective(int R, int op, int dtype,
                     for (int r = 0; r < R; ++r)
                         idx[r] = region_elem(src[r], j);
                     store_f32(out_bufs[d], dtype, region_elem(dp, j),
-                              fold_ranks(R, dtype, in_bufs, idx));
+                              fold_op(op, R, dtype, in_bufs, idx));
                 }
             }
         }

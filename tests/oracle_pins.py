@@ -355,6 +355,113 @@ def check_layout_pair_rejects(orc):
         raise AssertionError(f"accepted an invalid layout pair: {op} {lin} {lout}")
 
 
+# ------------------------------------------- fp16, 1-byte elements, maximum
+
+
+def _as16(vals):
+    return np.asarray(vals, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def check_fp16_rounding_vs_torch(orc):
+    """fp32 -> binary16 rounding equals PyTorch's CPU cast: every binary16 value,
+    every midpoint between neighbours (exact ties), points just beside them,
+    specials and a million random fp32 patterns."""
+    import torch
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = h.view(np.float16).astype(np.float64)
+    fin = np.isfinite(vals)
+    v = np.sort(np.unique(vals[fin]))
+    mids = (v[:-1] + v[1:]) / 2
+    pts = np.concatenate([v, mids, np.nextafter(mids.astype(np.float32), np.float32(np.inf)).astype(np.float64),
+                          np.nextafter(mids.astype(np.float32), np.float32(-np.inf)).astype(np.float64),
+                          [65504.0, 65519.99, 65520.0, 65536.0, 1e30, 2.0 ** -25, 2.0 ** -26, 3 * 2.0 ** -26]])
+    f = np.concatenate([pts.astype(np.float32), -pts.astype(np.float32)])
+    rng = np.random.default_rng(6)
+    f = np.concatenate([f, rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32).view(np.float32)])
+    mine = orc.f32_to_f16(f)
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.all(((mine[nan] & 0x7C00) == 0x7C00) & ((mine[nan] & 0x3FF) != 0))
+
+
+def check_fp16_sums(orc):
+    """fp16 sums: small integers are exact (numpy int64), and random sums stay
+    within recursive-summation error plus one binary16 rounding of fp64."""
+    R, n = 8, 4000
+    ints = [synth.int_uniform_f32(8, r, n) for r in range(R)]
+    exact = np.sum(np.stack([a.astype(np.int64) for a in ints]), axis=0)
+    out = orc.allreduce([_as16(a) for a in ints], "fp16")[0]
+    assert np.array_equal(out.view(np.float16).astype(np.int64), exact)
+    rs = orc.reducescatter([_as16(a) for a in ints], [500] * R, "fp16")
+    assert np.array_equal(rs[3].view(np.float16).astype(np.int64), exact[1500:2000])
+    x = [_as16(synth.normal_f32(12, r, n)) for r in range(R)]
+    xv = np.stack([a.view(np.float16).astype(np.float64) for a in x])
+    ex = xv.sum(axis=0)
+    gam = (R - 1) * 2.0 ** -24 / (1 - (R - 1) * 2.0 ** -24)
+    err = gam * np.abs(xv).sum(axis=0)
+    got = orc.allreduce(x, "fp16")[R - 1].view(np.float16).astype(np.float64)
+    assert np.all(np.abs(got - ex) <= err + 2.0 ** -11 * (np.abs(ex) + err) + 2.0 ** -25)
+
+
+def check_max(orc):
+    """The maximum against numpy's maximum.reduce on data without zeros or NaN,
+    the Figure 4 sentinels (rank 2 holds every maximum), and the rank-order
+    rules for signed zeros and NaN."""
+    for dt, conv in (("fp32", lambda a: a), ("bf16", lambda a: _as("bf16", a)), ("fp16", _as16)):
+        R, n = 5, 3000
+        raw = [synth.normal_f32(13, r, n) for r in range(R)]
+        ins = [conv(a) for a in raw]
+        vals = np.stack([(_vals(dt, a) if dt != "fp16" else a.view(np.float16).astype(np.float64)) for a in ins])
+        want = np.maximum.reduce(vals, axis=0)
+        got = orc.allreduce(ins, dt, op="max")[2]
+        gotv = _vals(dt, got) if dt != "fp16" else got.view(np.float16).astype(np.float64)
+        assert np.array_equal(gotv, want), dt
+        lens = [600, 0, 1200, 1, 1199]
+        rs = orc.reducescatter(ins, lens, dt, op="max")
+        o = 0
+        for k in range(R):
+            gk = _vals(dt, rs[k]) if dt != "fp16" else rs[k].view(np.float16).astype(np.float64)
+            assert np.array_equal(gk, want[o:o + lens[k]]), (dt, k)
+            o += lens[k]
+    g = load_golden("fig4_three_ranks.txt")
+    ins = [_as("fp32", g["input"][r]) for r in range(3)]
+    rs = orc.reducescatter(ins, [2, 2, 2], "fp32", op="max")
+    assert [list(r) for r in rs] == [[20, 21], [22, 23], [24, 25]]
+    z = [np.array([-0.0, 0.0, np.nan, 1.0], np.float32), np.array([0.0, -0.0, 7.0, np.nan], np.float32)]
+    out = orc.allreduce(z, "fp32", op="max")[1]
+    assert out.view(np.uint32)[0] == 0x80000000 and out.view(np.uint32)[1] == 0
+    assert np.isnan(out[2]) and out[3] == 1.0
+
+
+def check_one_byte_elements(orc):
+    """1-byte (fp8) elements move bit for bit (numpy concatenate / split) and are never reduced."""
+    R = 4
+    rng = np.random.default_rng(14)
+    lens = [5, 0, 17, 3]
+    ins = [rng.integers(0, 256, size=n, dtype=np.uint8) for n in lens]
+    for out in orc.allgather(ins, "fp8"):
+        assert np.array_equal(out, np.concatenate(ins))
+    m = [[(r + j) % 3 + r for j in range(R)] for r in range(R)]
+    ins = [rng.integers(0, 256, size=sum(m[r]), dtype=np.uint8) for r in range(R)]
+    pieces = [np.split(ins[r], np.cumsum(m[r])[:-1]) for r in range(R)]
+    outs = orc.alltoall(ins, m, "fp8")
+    for j in range(R):
+        assert np.array_equal(outs[j], np.concatenate([pieces[r][j] for r in range(R)]))
+    for call in (lambda: orc.allreduce(ins[:1], "fp8"), lambda: orc.reducescatter(ins[:1], [sum(m[0])], "fp8")):
+        try:
+            call()
+        except ValueError:
+            continue
+        raise AssertionError("1-byte elements were reduced")
+    try:
+        orc.collective("sum", "fp8", [[(0, 0, 4)]], [[(0, 0, 4)]], [np.zeros(4, np.uint8)], [4])
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("the layout-pair definition reduced 1-byte elements")
+
+
 ALL_CHECKS = [
     check_fig4_golden,
     check_v_golden,
@@ -369,4 +476,8 @@ ALL_CHECKS = [
     check_bruteforce,
     check_layout_pair_definition,
     check_layout_pair_rejects,
+    check_fp16_rounding_vs_torch,
+    check_fp16_sums,
+    check_max,
+    check_one_byte_elements,
 ]

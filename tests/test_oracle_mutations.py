@@ -17,8 +17,9 @@ import oracle.build as obuild
 MUTATIONS = {
     "fold_drops_last_rank": ("for (int r = 1; r < R; ++r)\n        acc = acc +",
                              "for (int r = 1; r < R - 1; ++r)\n        acc = acc +"),
-    "fold_starts_from_plus_zero": ("float acc = load_f32(bufs[0], dtype, idx[0]);\n    for (int r = 1;",
-                                   "float acc = 0.0f;\n    for (int r = 0;"),
+    "fold_starts_from_plus_zero": ("float acc = load_f32(bufs[0], dtype, idx[0]);\n    for (int r = 1; r < R; ++r)\n"
+                                   "        acc = acc +",
+                                   "float acc = 0.0f;\n    for (int r = 0; r < R; ++r)\n        acc = acc +"),
     "fold_reverse_order": ("float acc = load_f32(bufs[0], dtype, idx[0]);\n    for (int r = 1; r < R; ++r)\n"
                            "        acc = acc + load_f32(bufs[r], dtype, idx[r]);",
                            "float acc = load_f32(bufs[R - 1], dtype, idx[R - 1]);\n    for (int r = R - 2; r >= 0; --r)\n"
@@ -37,6 +38,11 @@ MUTATIONS = {
                                    "in[r], (s * H + h * (uint64_t)R + j) * D + d"),
     "layout_region_ignores_stride": ("return p->offset + (j / p->len) * p->row_stride + (j % p->len);",
                                      "return p->offset + j;"),
+    "max_keeps_later_ties": ("        if (v > acc)\n            acc = v;", "        if (v >= acc)\n            acc = v;"),
+    "max_is_min": ("        if (v > acc)\n            acc = v;", "        if (v < acc)\n            acc = v;"),
+    "f16_ties_away_from_zero": ("        n = fmod(t, 2.0) == 0.0 ? t : t + 1.0;", "        n = t + 1.0;"),
+    "f16_wrong_subnormal_spacing": ("        ulp = ldexp(1.0, -24);\n    } else {", "        ulp = ldexp(1.0, -25);\n    } else {"),
+    "f16_no_overflow_to_inf": ("    if (v >= 65536.0)\n        return (uint16_t)(sign | 0x7C00u);", "    if (v > 1e300)\n        return (uint16_t)(sign | 0x7C00u);"),
     "layout_sum_accepts_any_rank_order": ("if (src_rank[r] != r || region_count(src[r]) != cnt)",
                                           "if (region_count(src[r]) != cnt)"),
 }
