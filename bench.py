@@ -84,7 +84,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("atom.cu", "snac.h"):
+    for f in ("atom_impl.cuh", "atom.cu", "snac.h"):
         with open(os.path.join(ROOT, "copy_reduce_datapath_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -501,19 +501,29 @@ def run_ours(args):
 # ------------------------------------------------------------ single cases
 
 CASES = {
-    # name: (collective, dtype, description)
-    "allgather": ("allgather", "bf16", "AllGather, R=8, bf16 N(0,1), equal partitions, T = output bytes per rank"),
-    "allreduce": ("allreduce", "bf16", "AllReduce, R=8, bf16 N(0,1), T = bytes per rank"),
-    "allreduce_r3_fp32": ("allreduce", "fp32", "AllReduce, R=3, fp32 integers in [-8, 8], T = bytes per rank"),
-    "reducescatter_bf16": ("reducescatter", "bf16", "ReduceScatter, R=8, bf16 U(-1,1), T = input bytes per rank"),
-    "reducescatter_fp32": ("reducescatter", "fp32", "ReduceScatter, R=8, fp32 U(-1,1), T = input bytes per rank"),
-    "reducescatter_inplace_bf16": ("reducescatter_inplace", "bf16", "ReduceScatter in place, R=8, bf16 U(-1,1)"),
-    "alltoall_moe": ("alltoall", "bf16", "AllToAll, R=8, per rank [4096 tokens, 7168] bf16, 8 token groups (T ignored)"),
-    "ulysses": ("ulysses", "bf16", "Ulysses AllToAll, R=8, per rank [16384, 32, 128] bf16, seq->head (T ignored)"),
-    "allgatherv": ("allgatherv", "bf16", "AllGatherV, R=8, bf16, Zipf s=0.125 lengths, T = output bytes per rank"),
-    "reducescatterv": ("reducescatterv", "bf16", "ReduceScatterV, R=8, bf16, Zipf s=0.125, T = input bytes per rank"),
-    "alltoallv": ("alltoallv", "bf16", "AllToAllV, R=8, bf16, Zipf s=0.125 rows, T = input bytes per rank"),
+    # name: (collective, dtype, reduction, description)
+    "allgather": ("allgather", "bf16", "sum", "AllGather, R=8, bf16 N(0,1), equal partitions, T = output bytes per rank"),
+    "allreduce": ("allreduce", "bf16", "sum", "AllReduce, R=8, bf16 N(0,1), T = bytes per rank"),
+    "allreduce_r3_fp32": ("allreduce", "fp32", "sum", "AllReduce, R=3, fp32 integers in [-8, 8], T = bytes per rank"),
+    "reducescatter_bf16": ("reducescatter", "bf16", "sum", "ReduceScatter, R=8, bf16 U(-1,1), T = input bytes per rank"),
+    "reducescatter_fp32": ("reducescatter", "fp32", "sum", "ReduceScatter, R=8, fp32 U(-1,1), T = input bytes per rank"),
+    "reducescatter_inplace_bf16": ("reducescatter_inplace", "bf16", "sum", "ReduceScatter in place, R=8, bf16 U(-1,1)"),
+    "alltoall_moe": ("alltoall", "bf16", "sum", "AllToAll, R=8, per rank [4096 tokens, 7168] bf16, 8 token groups (T ignored)"),
+    "ulysses": ("ulysses", "bf16", "sum", "Ulysses AllToAll, R=8, per rank [16384, 32, 128] bf16, seq->head (T ignored)"),
+    "allgatherv": ("allgatherv", "bf16", "sum", "AllGatherV, R=8, bf16, Zipf s=0.125 lengths, T = output bytes per rank"),
+    "reducescatterv": ("reducescatterv", "bf16", "sum", "ReduceScatterV, R=8, bf16, Zipf s=0.125, T = input bytes per rank"),
+    "alltoallv": ("alltoallv", "bf16", "sum", "AllToAllV, R=8, bf16, Zipf s=0.125 rows, T = input bytes per rank"),
+    # further element types and the maximum reduction
+    "allreduce_fp16": ("allreduce", "fp16", "sum", "AllReduce, R=8, fp16 U(-1,1), T = bytes per rank"),
+    "reducescatter_fp16": ("reducescatter", "fp16", "sum", "ReduceScatter, R=8, fp16 U(-1,1), T = input bytes per rank"),
+    "allreduce_max_bf16": ("allreduce", "bf16", "max", "AllReduce (maximum), R=8, bf16 N(0,1), T = bytes per rank"),
+    "allreduce_max_fp32": ("allreduce", "fp32", "max", "AllReduce (maximum), R=8, fp32 U(-1,1), T = bytes per rank"),
+    "allgather_fp8": ("allgather", "fp8", "sum", "AllGather, R=8, one-byte elements, T = output bytes per rank"),
+    "alltoall_moe_fp8": ("alltoall", "fp8", "sum", "AllToAll, R=8, per rank [4096 tokens, 7168] fp8, 8 token groups (T ignored)"),
+    "allgatherv_fp8": ("allgatherv", "fp8", "sum", "AllGatherV, R=8, one-byte elements, Zipf s=0.125, T = output bytes per rank"),
 }
+TORCH_DT = {"bf16": "bfloat16", "fp32": "float32", "fp16": "float16", "fp8": "uint8"}
+ELEM_BYTES = {"bf16": 2, "fp32": 4, "fp16": 2, "fp8": 1}
 
 
 def run_case(args):
@@ -523,11 +533,11 @@ def run_case(args):
     import __graft_entry__
     __graft_entry__.build()
     from copy_reduce_datapath_gb300 import purlin as P
-    kind, dt, desc = CASES[args.case]
+    kind, dt, red, desc = CASES[args.case]
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
-    S = 2 if dt == "bf16" else 4
+    tdt = getattr(torch, TORCH_DT[dt])
+    S = ELEM_BYTES[dt]
     pol = P.pl_policy_default()
     for kv in filter(None, args.policy.split(",")):
         k, v = kv.split("=")
@@ -538,8 +548,11 @@ def run_case(args):
     N = T // S
 
     def normal(seed, r, n):
-        return synth.device_normal_bf16(seed, r, n, dev) if dt == "bf16" else \
-            synth.device_uniform_pm1(seed, r, n, dev, tdt)
+        if dt == "bf16":
+            return synth.device_normal_bf16(seed, r, n, dev)
+        if dt == "fp8":
+            return synth.device_bytes(seed, r, n, dev)
+        return synth.device_uniform_pm1(seed, r, n, dev, tdt)
 
     if kind == "allgather":
         n = N // Rr
@@ -548,23 +561,24 @@ def run_case(args):
         lin, lout, op = P.pl_layout_rank_owned(Rr, [n] * Rr), P.pl_layout_partitioned(Rr, [n] * Rr), "copy"
         moved = (n * Rr + Rr * n * Rr) * S
     elif kind == "allreduce":
-        if dt == "fp32":
+        if args.case == "allreduce_r3_fp32":
             ins = [torch.from_numpy(synth.int_uniform_f32(0, r, N)).to(dev) for r in range(Rr)]
         else:
             ins = [normal(1, 100 + r, N) for r in range(Rr)]
         outs = [torch.empty(N, dtype=tdt, device=dev) for _ in range(Rr)]
         lin = lout = P.pl_layout_partitioned(Rr, synth.equal_lengths(N, Rr))
-        op, moved = "sum", 2 * Rr * N * S
+        op, moved = red, 2 * Rr * N * S
     elif kind in ("reducescatter", "reducescatter_inplace", "reducescatterv"):
         lens = synth.zipf_lengths(N, Rr, 0.125, seed=4) if kind == "reducescatterv" else [N // Rr] * Rr
-        ins = [synth.device_uniform_pm1(2, r, N, dev, tdt) for r in range(Rr)]
+        ins = [normal(2, r, N) for r in range(Rr)] if dt == "fp8" else \
+            [synth.device_uniform_pm1(2, r, N, dev, tdt) for r in range(Rr)]
         lin = P.pl_layout_partitioned(Rr, lens)
         if kind == "reducescatter_inplace":
             outs, lout = ins, P.pl_layout_rank_owned_inplace(Rr, lens)
         else:
             outs = [torch.empty(lens[k], dtype=tdt, device=dev) for k in range(Rr)]
             lout = P.pl_layout_rank_owned(Rr, lens)
-        op, moved = "sum", (Rr * N + N) * S
+        op, moved = red, (Rr * N + N) * S
     elif kind == "allgatherv":
         lens = synth.zipf_lengths(N, Rr, 0.125, seed=4)
         ins = [normal(4, r, lens[r]) for r in range(Rr)]

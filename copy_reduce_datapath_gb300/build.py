@@ -1,6 +1,6 @@
 """Build libpurlin1.so in-tree for sm_103a with nvcc (no CMake, no PyTorch extension).
 
-The two translation units compile in parallel and are linked into
+The translation units compile in parallel and are linked into
 copy_reduce_datapath_gb300/libpurlin1.so.  The CUDA runtime is linked
 statically, so the library loads on a machine without a GPU (the ABI export
 checks run there); every entry point that touches the GPU returns
@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
           f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["runtime.cpp", "atom.cu", "noalloc.cu"]
+SOURCES = ["runtime.cpp", "atom.cu", "atom_fp16.cu", "atom_fp32.cu", "atom_fp8.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -1,945 +1,15 @@
-// The Atom datapath and the device side of SNAC for sm_103a.
-//
-// "Purlin: Separating Orchestration from the Datapath of Collectives":
-//   - abstract: the Atom provides the two data-movement primitives of
-//     collectives, copy and reduce; SNAC (Stage, Notify, And Consume) is the
-//     orchestration above it;
-//   - Table 1 ("Compatibility"): a datapath built on vectorised loads and
-//     stores; Figure 11 caption: a pipelined copy with 1 to 8 stages.
-//
-// One persistent kernel executes a work list (see snac.h).  Every work item
-// is "wait on flags -> move -> notify / credit flags", and the move is either
-// a copy of one source into up to 64 destinations or the fp32 sum, in rank
-// order, of up to 64 sources written to up to 64 destinations.  Items are
-// claimed in index order (a device counter) whenever an item waits on another,
-// so a waiting CTA only ever waits for items that were claimed before it and
-// are therefore running: the grid makes progress without co-residency.  Every
-// wait is bounded by a timeout on %globaltimer and an iteration cap; a wait
-// that gives up records PL_ERR_TIMEOUT in the status word and raises an abort
-// flag that makes every other wait give up too, so the kernel always returns.
-#include "snac.h"
-
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
-#include <cstdint>
+// Launch of the persistent SNAC kernel: picks the element type's
+// instantiation (this file holds the bf16 one; atom_fp16.cu, atom_fp32.cu and
+// atom_fp8.cu the others, compiled in parallel) and whether the plan may use
+// the kernels without realigning bodies.
+#include "atom_impl.cuh"
 
 namespace purlin {
-namespace {
 
-constexpr int kStatusTimeout = 6;  // PL_ERR_TIMEOUT
-constexpr int kCtasPerSm = 1;  // 512 threads with up to 128 registers each
-constexpr int kCopyUnroll = 8; // 16-byte vectors a thread keeps in flight in the copy bodies
-
-// ------------------------------------------------------- memory-model helpers
-
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
+cudaError_t launch_snac_bf16(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s)
 {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
+    return launch_dtype<kDtBf16>(a, ctas, bulk, aligned, stages, s);
 }
-
-__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
-{
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v)
-{
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void st_relaxed_u32(unsigned int* p, unsigned int v)
-{
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_relaxed_s32(const int* p)
-{
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ unsigned long long global_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Streaming 16-byte load that is served from L2 (data may have been written
-// by another CTA of this launch after a flag acquire).
-__device__ __forceinline__ uint4 ld16(const char* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
-#if defined(PL_STORE_STREAMING)
-// Developer build option: evict-first stores for outputs nobody rereads.
-__device__ __forceinline__ void st16(char* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
-#else
-__device__ __forceinline__ void st16(char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
-#endif
-
-// ------------------------------------------------------------- bounded waits
-
-__device__ void give_up(const LaunchArgs& a)
-{
-    atomicCAS(a.st.status, 0, kStatusTimeout);
-    atomicExch(a.st.abort, 1);
-}
-
-// Waits until *flag >= target.  false: the wait expired or another wait did.
-__device__ bool wait_at_least(const unsigned long long* flag, unsigned long long target, const LaunchArgs& a)
-{
-    const unsigned long long t0 = global_ns();
-    // The cap bounds the loop even if %globaltimer stalled: every iteration
-    // sleeps, and 2^26 iterations exceed any sensible timeout.
-    const unsigned int cap = 1u << 26;
-    for (unsigned int it = 0; it < cap; ++it) {
-        if (ld_acquire(flag) >= target)
-            return true;
-        if ((it & 31) == 31) {
-            if (ld_relaxed_s32(a.st.abort))
-                return false;
-            if (global_ns() - t0 > a.timeout_ns)
-                break;
-        }
-        __nanosleep(it < 64 ? 32 : 256);
-    }
-    give_up(a);
-    return false;
-}
-
-__device__ __forceinline__ unsigned long long tag(const LaunchArgs& a, unsigned int use)
-{
-    return (a.epoch << 24) | (unsigned long long)(use + 1u);
-}
-
-// Warp 0 of the CTA: every wait of the item, one flag per lane (lanes take
-// flags lane, lane + 32, ...), so an item's waits overlap instead of costing
-// one round trip each.  Returns, in every lane, whether all waits passed.
-__device__ bool run_waits(const LaunchArgs& a, const Item& it, int lane)
-{
-    bool ok = ld_relaxed_s32(a.st.abort) == 0;
-    for (unsigned k = (unsigned)lane; ok && k < it.nwait; k += 32) {
-        const Sync s = a.syncs[it.sync + k];
-        const unsigned long long* f = s.type == kWaitFull ? a.st.full + s.flag : a.st.done + s.flag;
-        ok = wait_at_least(f, tag(a, s.use), a);
-    }
-    return __all_sync(0xffffffffu, ok) != 0;
-}
-
-// Warp 0 of the CTA, after a barrier that follows the item's stores: the
-// notifies and credits of the item, one flag per lane.  Each posting lane
-// fences the CTA's writes (ordered before it by the barrier) ahead of its
-// release.
-__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index, int lane)
-{
-    for (unsigned k = (unsigned)lane; k < it.npost; k += 32) {
-        const Sync s = a.syncs[it.sync + it.nwait + k];
-        __threadfence();
-        if (s.type == kNotify) {
-            if ((long long)index == a.drop_notify)
-                continue;  // test hook: consumers of this item will time out
-            st_release(a.st.full + s.flag, tag(a, s.use));
-        } else if (s.type == kCredit) {
-            unsigned old = atom_add_acq_rel(a.st.count + s.flag, 1u);
-            if (old + 1u == s.count) {
-                st_relaxed_u32(a.st.count + s.flag, 0u);
-                st_release(a.st.done + s.flag, tag(a, s.use));
-            }
-        }
-    }
-}
-
-// ------------------------------------------------- bulk-copy (TMA) primitives
-
-constexpr unsigned kBulkPiece = 16384;  // bytes per ring stage
-constexpr unsigned kBulkMin = 4096;     // smaller bodies use the vector path
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
-// Global -> shared bulk copy that completes `bytes` transactions on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* smem, const void* g, unsigned bytes, unsigned long long* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(smem)),
-                 "l"(g), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-// Shared -> global bulk copy in the current bulk group.
-__device__ __forceinline__ void bulk_s2g(void* g, const void* smem, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(smem_u32(smem)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-// Bounded wait for the phase `parity` of an mbarrier.
-__device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const LaunchArgs& a)
-{
-    const unsigned long long t0 = global_ns();
-    for (unsigned it = 0; it < (1u << 26); ++it) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if ((it & 255) == 255 && global_ns() - t0 > a.timeout_ns)
-            break;
-    }
-    give_up(a);
-    return false;
-}
-
-// The CTA's bulk-copy ring: `stages` buffers of kBulkPiece bytes, one mbarrier
-// each.  Only thread 0 touches it; `phase` holds the parity each stage's
-// barrier will complete next.
-struct BulkRing {
-    char* buf;
-    unsigned long long* bar;
-    int stages;
-    unsigned phase;
-};
-
-// ------------------------------------------------------------- element math
-
-template <int S> struct Elem;
-
-template <> struct Elem<2> {  // bf16
-    static __device__ __forceinline__ float to_f(uint32_t h) { return __uint_as_float(h << 16); }
-    static __device__ __forceinline__ uint32_t from_f(float f)
-    {
-        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
-    }
-    static __device__ __forceinline__ uint32_t load(const char* p) { return __ldcg(reinterpret_cast<const unsigned short*>(p)); }
-    static __device__ __forceinline__ void store(char* p, uint32_t v) { *reinterpret_cast<unsigned short*>(p) = (unsigned short)v; }
-};
-
-template <> struct Elem<4> {  // fp32
-    static __device__ __forceinline__ float to_f(uint32_t w) { return __uint_as_float(w); }
-    static __device__ __forceinline__ uint32_t from_f(float f) { return __float_as_uint(f); }
-    static __device__ __forceinline__ uint32_t load(const char* p) { return __ldcg(reinterpret_cast<const unsigned int*>(p)); }
-    static __device__ __forceinline__ void store(char* p, uint32_t v) { *reinterpret_cast<unsigned int*>(p) = v; }
-};
-
-// Accumulators of one 16-byte vector: 8 bf16 or 4 fp32 lanes.
-template <int S> struct Acc {
-    static constexpr int N = 16 / S;
-    float v[N];
-    __device__ __forceinline__ void set(uint4 x)
-    {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (S == 2) {
-                v[2 * i] = Elem<2>::to_f(w[i] & 0xFFFFu);
-                v[2 * i + 1] = Elem<2>::to_f(w[i] >> 16);
-            } else {
-                v[i] = Elem<4>::to_f(w[i]);
-            }
-        }
-    }
-    __device__ __forceinline__ void add(uint4 x)
-    {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (S == 2) {
-                v[2 * i] = __fadd_rn(v[2 * i], Elem<2>::to_f(w[i] & 0xFFFFu));
-                v[2 * i + 1] = __fadd_rn(v[2 * i + 1], Elem<2>::to_f(w[i] >> 16));
-            } else {
-                v[i] = __fadd_rn(v[i], Elem<4>::to_f(w[i]));
-            }
-        }
-    }
-    __device__ __forceinline__ uint4 pack() const
-    {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (S == 2)
-                w[i] = Elem<2>::from_f(v[2 * i]) | (Elem<2>::from_f(v[2 * i + 1]) << 16);
-            else
-                w[i] = Elem<4>::from_f(v[i]);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-
-// The 16 bytes that start q bytes into the 32-byte pair (lo, hi); q is even.
-__device__ __forceinline__ uint4 realign(uint4 lo, uint4 hi, int q)
-{
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    const int k = q >> 2;
-    const unsigned sh = (unsigned)(q & 3) * 8u;
-    uint32_t r[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const uint32_t a0 = k == 0 ? w[m] : k == 1 ? w[m + 1] : k == 2 ? w[m + 2] : w[m + 3];
-        const uint32_t a1 = k == 0 ? w[m + 1] : k == 1 ? w[m + 2] : k == 2 ? w[m + 3] : w[m + 4];
-        r[m] = __funnelshift_r(a0, a1, sh);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
-}
-
-// ------------------------------------------------------------ the datapath
-
-// Per-item shared state: byte pointers of row 0 and byte strides between rows.
-struct ItemShared {
-    const char* src[kMaxRanks];
-    char* dst[kMaxRanks];
-    unsigned long long sstride[kMaxRanks];
-    unsigned long long dstride[kMaxRanks];
-};
-
-// Row pointer of source s / destination d.
-#define SRC_ROW(sh, s, row) ((sh).src[s] + (size_t)(row) * (sh).sstride[s])
-#define DST_ROW(sh, d, row) ((sh).dst[d] + (size_t)(row) * (sh).dstride[d])
-
-// Copy of nv 16-byte vectors from one source to every destination in `mask`.
-// The destinations are 16-byte aligned at `body`; the source is `q` bytes past
-// a 16-byte boundary (QALIGNED: q == 0).  U vectors in flight per thread.
-template <bool QALIGNED, int U>
-__device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
-                                       unsigned nv, int tid, int nthr)
-{
-    const char* src = SRC_ROW(sh, 0, row) + body;
-    const int q = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
-    const char* base = src - q;
-    const unsigned step = (unsigned)nthr * U;
-    for (unsigned v0 = tid; v0 < nv; v0 += step) {
-        uint4 x[U];
-        if constexpr (QALIGNED) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                if (v < nv)
-                    x[u] = ld16(base + (size_t)v * 16);
-            }
-        } else {
-            uint4 lo[U], hi[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                if (v < nv) {
-                    lo[u] = ld16(base + (size_t)v * 16);
-                    hi[u] = ld16(base + (size_t)v * 16 + 16);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                x[u] = realign(lo[u], hi[u], q);
-        }
-#pragma unroll 1
-        for (unsigned long long m = mask; m; m &= m - 1) {
-            const int d = __ffsll((long long)m) - 1;
-            char* dst = DST_ROW(sh, d, row) + body;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                if (v < nv)
-                    st16(dst + (size_t)v * 16, x[u]);
-            }
-        }
-    }
-}
-
-// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
-// to every destination in `mask`.  G sources in flight per thread.
-// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
-// to every destination in `mask`.  Aligned sources: U vectors x G sources
-// (U * G = 8 loads) in flight per thread, U chosen from the source count so
-// that few sources still keep the memory system busy.  Sources at mixed
-// misalignments (rare) are loaded one at a time and realigned.
-template <int S, int U>
-__device__ __forceinline__ void sum_aligned(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                            size_t body, unsigned nv, int tid, int nthr)
-{
-    constexpr int G = 8 / U;
-    const unsigned step = (unsigned)nthr * U;
-    for (unsigned v0 = tid; v0 < nv; v0 += step) {
-        Acc<S> acc[U];
-        for (int s0 = 0; s0 < nsrc; s0 += G) {
-            uint4 x[U][G];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if (s0 + g < nsrc && v < nv)
-                        x[u][g] = ld16(SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (s0 + g < nsrc) {
-                        if (s0 + g == 0)
-                            acc[u].set(x[u][g]);
-                        else
-                            acc[u].add(x[u][g]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const unsigned v = v0 + u * nthr;
-            if (v < nv) {
-                const uint4 out = acc[u].pack();
-#pragma unroll 1
-                for (unsigned long long m = mask; m; m &= m - 1) {
-                    const int d = __ffsll((long long)m) - 1;
-                    st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, out);
-                }
-            }
-        }
-    }
-}
-
-template <int S>
-__device__ __forceinline__ void sum_mixed(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                          size_t body, unsigned nv, int tid, int nthr)
-{
-    for (unsigned v = tid; v < nv; v += nthr) {
-        Acc<S> acc;
-        for (int s = 0; s < nsrc; ++s) {
-            const char* p = SRC_ROW(sh, s, row) + body + (size_t)v * 16;
-            const int q = (int)(reinterpret_cast<uintptr_t>(p) & 15u);
-            const uint4 lo = ld16(p - q);
-            const uint4 x = q ? realign(lo, ld16(p - q + 16), q) : lo;
-            if (s == 0)
-                acc.set(x);
-            else
-                acc.add(x);
-        }
-        const uint4 out = acc.pack();
-#pragma unroll 1
-        for (unsigned long long m = mask; m; m &= m - 1) {
-            const int d = __ffsll((long long)m) - 1;
-            st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, out);
-        }
-    }
-}
-
-template <int S, bool WIDE>
-__device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                         size_t body, unsigned nv, int tid, int nthr)
-{
-    // 8 loads in flight per thread either way: 1 vector x 8 sources when every
-    // sum has 8 or more sources, else 2 vectors x 4 sources.
-    sum_aligned<S, WIDE ? 1 : 2>(sh, nsrc, mask, row, body, nv, tid, nthr);
-}
-
-// Thread 0: copies `nbytes` (a multiple of 16, both ends 16-byte aligned)
-// from `src` to every destination in `mask` through the ring.  Loads run up
-// to `stages` pieces ahead; a stage is refilled once the stores that read it
-// have finished reading.  Returns with every store complete.
-__device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
-                          const char* src, unsigned nbytes, const LaunchArgs& a)
-{
-    const unsigned np = (nbytes + kBulkPiece - 1) / kBulkPiece;
-    const unsigned st = (unsigned)bk.stages;
-    fence_proxy_async();  // order earlier generic writes (after a flag acquire) before the async loads
-    unsigned issued = 0;
-    auto load = [&](unsigned q) {
-        const unsigned sidx = q % st;
-        const unsigned bytes = min(kBulkPiece, nbytes - q * kBulkPiece);
-        mbar_expect_tx(&bk.bar[sidx], bytes);
-        bulk_g2s(bk.buf + (size_t)sidx * kBulkPiece, src + (size_t)q * kBulkPiece, bytes, &bk.bar[sidx]);
-    };
-    for (; issued < np && issued < st; ++issued)
-        load(issued);
-    bool ok = true;
-    unsigned p = 0;
-    for (; p < np; ++p) {
-        const unsigned sidx = p % st;
-        if (st == 1 && p >= 1) {
-            bulk_wait_read0();
-            load(p);
-            issued = p + 1;
-        }
-        ok = mbar_wait(&bk.bar[sidx], (bk.phase >> sidx) & 1u, a);
-        if (!ok)
-            break;
-        bk.phase ^= 1u << sidx;
-        const unsigned bytes = min(kBulkPiece, nbytes - p * kBulkPiece);
-#pragma unroll 1
-        for (unsigned long long m = mask; m; m &= m - 1) {
-            const int d = __ffsll((long long)m) - 1;
-            bulk_s2g(DST_ROW(sh, d, row) + body + (size_t)p * kBulkPiece, bk.buf + (size_t)sidx * kBulkPiece, bytes);
-        }
-        bulk_commit();
-        if (st > 1 && p >= 1 && issued < np) {
-            bulk_wait_read1();  // the stores of piece p-1 have read their stage
-            load(issued);
-            ++issued;
-        }
-    }
-    if (!ok) {
-        // A load never completed in time: wait (bounded) for every load still in
-        // flight so no copy lands in shared memory after this CTA moves on.
-        for (unsigned q = p; q < issued; ++q) {
-            const unsigned sidx = q % st;
-            if (mbar_wait(&bk.bar[sidx], (bk.phase >> sidx) & 1u, a))
-                bk.phase ^= 1u << sidx;
-        }
-    }
-    bulk_wait_all();
-    fence_proxy_async();  // the async-proxy stores before the generic release that follows
-}
-
-// Every source of the segment sits the same q bytes (q != 0) past a 16-byte
-// boundary while the destinations are 16-byte aligned at `body`.  Each warp
-// step loads 32 consecutive aligned vectors of every source (one per lane),
-// adds them lane by lane (sum), and lanes 0..30 splice their result with the
-// next lane's into one destination vector: 31 outputs per 32 loaded vectors,
-// one load per source per vector and one realignment per output.  Aligned
-// vector nv is the last one that holds bytes of the row.
-template <int S, bool SUM>
-__device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                             size_t body, unsigned nv, int q, int tid, int nthr)
-{
-    constexpr int U = SUM ? 2 : 8;  // warp steps in flight per thread
-    constexpr int G = 4;            // sources in flight per step (sum)
-    const int lane = tid & 31;
-    const unsigned warp = (unsigned)tid >> 5;
-    const unsigned span = 31u * ((unsigned)nthr >> 5);
-    for (unsigned g0 = warp * 31u; g0 < nv; g0 += span * U) {
-        uint4 r[U];
-        if constexpr (!SUM) {
-            const char* base = SRC_ROW(sh, 0, row) + body - q;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned idx = g0 + u * span + lane;
-                r[u] = idx <= nv ? ld16(base + (size_t)idx * 16) : make_uint4(0, 0, 0, 0);
-            }
-        } else {
-            Acc<S> acc[U];
-            for (int s0 = 0; s0 < nsrc; s0 += G) {
-                uint4 x[U][G];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const unsigned idx = g0 + u * span + lane;
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        x[u][g] = (s0 + g < nsrc && idx <= nv)
-                                      ? ld16(SRC_ROW(sh, s0 + g, row) + body - q + (size_t)idx * 16)
-                                      : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        if (s0 + g < nsrc) {
-                            if (s0 + g == 0)
-                                acc[u].set(x[u][g]);
-                            else
-                                acc[u].add(x[u][g]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                r[u] = acc[u].pack();
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            uint4 nb;
-            nb.x = __shfl_down_sync(0xffffffffu, r[u].x, 1);
-            nb.y = __shfl_down_sync(0xffffffffu, r[u].y, 1);
-            nb.z = __shfl_down_sync(0xffffffffu, r[u].z, 1);
-            nb.w = __shfl_down_sync(0xffffffffu, r[u].w, 1);
-            const unsigned out = g0 + u * span + lane;
-            if (lane < 31 && out < nv) {
-                const uint4 v = realign(r[u], nb, q);
-#pragma unroll 1
-                for (unsigned long long m = mask; m; m &= m - 1) {
-                    const int d = __ffsll((long long)m) - 1;
-                    st16(DST_ROW(sh, d, row) + body + (size_t)out * 16, v);
-                }
-            }
-        }
-    }
-}
-
-// A multi-row block whose rows are whole 16-byte vectors at 16-byte aligned
-// addresses in every source and destination: one flat index over
-// rows x vectors-per-row spread over the whole CTA (no per-row heads, tails
-// or realignment).
-template <int S, bool SUM, int U>
-__device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int ndst, unsigned rows, unsigned vpr,
-                                            int tid, int nthr)
-{
-    const unsigned total = rows * vpr;
-    if constexpr (!SUM) {
-        for (unsigned v0 = tid; v0 < total; v0 += (unsigned)nthr * U) {
-            uint4 x[U];
-            unsigned rr[U], cc[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                rr[u] = v / vpr;
-                cc[u] = v - rr[u] * vpr;
-                if (v < total)
-                    x[u] = ld16(SRC_ROW(sh, 0, rr[u]) + (size_t)cc[u] * 16);
-            }
-#pragma unroll 1
-            for (int d = 0; d < ndst; ++d) {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (v0 + u * nthr < total)
-                        st16(DST_ROW(sh, d, rr[u]) + (size_t)cc[u] * 16, x[u]);
-            }
-        }
-    } else {
-        constexpr int G = 8;
-        for (unsigned v = tid; v < total; v += nthr) {
-            const unsigned rr = v / vpr;
-            const unsigned cc = v - rr * vpr;
-            Acc<S> acc;
-            for (int s0 = 0; s0 < nsrc; s0 += G) {
-                uint4 x[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if (s0 + g < nsrc)
-                        x[g] = ld16(SRC_ROW(sh, s0 + g, rr) + (size_t)cc * 16);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (s0 + g < nsrc) {
-                        if (s0 + g == 0)
-                            acc.set(x[g]);
-                        else
-                            acc.add(x[g]);
-                    }
-                }
-            }
-            const uint4 out = acc.pack();
-#pragma unroll 1
-            for (int d = 0; d < ndst; ++d)
-                st16(DST_ROW(sh, d, rr) + (size_t)cc * 16, out);
-        }
-    }
-}
-
-// One row segment of n elements, executed by `nthr` threads with index `tid`.
-// Destinations in `mask` share the same address mod 16 (`dcls`); their
-// stores are 16-byte aligned after a head of at most 16/S - 1 elements, and
-// the rest up to the last whole vector goes through the vector bodies.
-template <int S, int OPS, bool BULK, bool ALIGN>
-__device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
-                                        unsigned n, unsigned dcls, int tid, int nthr, BulkRing& bk,
-                                        const LaunchArgs& a)
-{
-    constexpr int E = 16 / S;
-    unsigned head = ((16u - dcls) & 15u) / S;
-    if (head > n)
-        head = n;
-    unsigned nv = (n - head) / E;
-    if (ALIGN) {
-        // Kernels built for plans the host proved 16-byte aligned have no
-        // realigning bodies; should a segment still be misaligned, it is moved
-        // element by element below (correct, slower).
-        for (int s = 0; s < nsrc; ++s)
-            if (((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + (size_t)head * S) & 15u) != 0)
-                nv = 0;
-    }
-    const unsigned tail0 = head + nv * E;
-    const unsigned ntail = n - tail0;
-
-    // Scalar head and tail elements (and, see above, misaligned rows of aligned kernels).
-    for (unsigned e = tid; e < head + ntail; e += nthr) {
-        const unsigned i = e < head ? e : tail0 + (e - head);
-        uint32_t v;
-        if (nsrc == 1) {
-            v = Elem<S>::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
-        } else {
-            float acc = Elem<S>::to_f(Elem<S>::load(SRC_ROW(sh, 0, row) + (size_t)i * S));
-#pragma unroll 1
-            for (int s = 1; s < nsrc; ++s)
-                acc = __fadd_rn(acc, Elem<S>::to_f(Elem<S>::load(SRC_ROW(sh, s, row) + (size_t)i * S)));
-            v = Elem<S>::from_f(acc);
-        }
-#pragma unroll 1
-        for (unsigned long long m = mask; m; m &= m - 1) {
-            const int d = __ffsll((long long)m) - 1;
-            Elem<S>::store(DST_ROW(sh, d, row) + (size_t)i * S, v);
-        }
-    }
-    if (nv == 0)
-        return;
-
-    const size_t body = (size_t)head * S;
-    // Misalignment of every source relative to the aligned destinations.
-    const int q0 = (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, 0, row)) + body) & 15u);
-    bool uniform = true;
-    for (int s = 1; s < nsrc; ++s)
-        uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
-    const bool aligned = uniform && q0 == 0;
-    if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1)) {
-        if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
-            if (tid == 0)
-                bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
-        } else if (ALIGN || aligned)
-            copy_body<true, kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
-        else
-            shifted_body<S, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
-    } else if (OPS & kOpsSum) {
-        if (ALIGN || aligned)
-            sum_body<S, (OPS & kOpsWide) != 0>(sh, nsrc, mask, row, body, nv, tid, nthr);
-        else if (uniform)
-            shifted_body<S, true>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
-        else
-            sum_mixed<S>(sh, nsrc, mask, row, body, nv, tid, nthr);
-    }
-}
-
-// Moves one rows x cols block.  A one-row block is spread over the whole CTA;
-// a multi-row block gives each warp whole rows.  Destinations are grouped by
-// address mod 16; each group is one pass over the sources.
-template <int S, int OPS, bool BULK, bool ALIGN>
-__device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
-                                          unsigned long long cols, BulkRing& bk, const LaunchArgs& a)
-{
-    if (rows > 1 && ((cols * S) & 15u) == 0) {
-        // Rows of whole vectors, every row start aligned in every reference?
-        bool flat = true;
-        for (int i = 0; i < nsrc; ++i)
-            flat &= ((reinterpret_cast<uintptr_t>(sh.src[i]) | sh.sstride[i]) & 15u) == 0;
-        for (int i = 0; i < ndst; ++i)
-            flat &= ((reinterpret_cast<uintptr_t>(sh.dst[i]) | sh.dstride[i]) & 15u) == 0;
-        if (flat) {
-            const unsigned vpr = (unsigned)(cols * S / 16);
-            if ((OPS & kOpsCopy) && (!(OPS & kOpsSum) || nsrc == 1))
-                flat2d_body<S, false, kCopyUnroll>(sh, 1, ndst, rows, vpr, (int)threadIdx.x,
-                                                                     (int)blockDim.x);
-            else if (OPS & kOpsSum)
-                flat2d_body<S, true, 1>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
-            return;
-        }
-    }
-    const bool one_row = rows == 1;
-    const int tid = one_row ? (int)threadIdx.x : (int)(threadIdx.x & 31);
-    const int nthr = one_row ? (int)blockDim.x : 32;
-    const unsigned r0 = one_row ? 0u : threadIdx.x >> 5;
-    const unsigned rstep = one_row ? 1u : blockDim.x >> 5;
-    for (unsigned r = r0; r < rows; r += rstep) {
-        unsigned long long todo = ndst >= 64 ? ~0ull : ((1ull << ndst) - 1ull);
-        while (todo) {
-            const int d0 = __ffsll((long long)todo) - 1;
-            const unsigned cls = (unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d0, r)) & 15u);
-            unsigned long long group = 0;
-            for (unsigned long long m = todo; m; m &= m - 1) {
-                const int d = __ffsll((long long)m) - 1;
-                if ((unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d, r)) & 15u) == cls)
-                    group |= 1ull << d;
-            }
-            todo &= ~group;
-            segment<S, OPS, BULK, ALIGN>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a);
-        }
-    }
-}
-
-// ------------------------------------------------------------- the kernel
-
-// Shared-memory image of one claimed work item: its index and its header.
-struct Slot {
-    unsigned index;
-    Item item;
-};
-
-// Thread 0: the next item index of this CTA (in index order through the
-// device ticket when items wait on one another, else round-robin).
-__device__ __forceinline__ unsigned claim(const LaunchArgs& a, unsigned k)
-{
-    return a.use_tickets ? atomicAdd(a.st.ticket, 1u) : blockIdx.x + k * gridDim.x;
-}
-
-// Region pointer of reference `tid` of `it` into `sh`.
-template <int S>
-__device__ __forceinline__ void put_ref(const LaunchArgs& a, const Item& it, const Ref& f, ItemShared& sh, int tid)
-{
-    char* base = a.bufs[f.buf] + f.offset * (unsigned long long)S;
-    const unsigned long long stride = f.stride * (unsigned long long)S;
-    if (tid < it.nsrc) {
-        sh.src[tid] = base;
-        sh.sstride[tid] = stride;
-    } else {
-        sh.dst[tid - it.nsrc] = base;
-        sh.dstride[tid - it.nsrc] = stride;
-    }
-}
-
-// The persistent SNAC kernel.  While item k moves, the region references of
-// item k+1 and the header of item k+2 are already in flight, so the work
-// list's metadata adds no round trips per item.  With tickets, a CTA holds
-// at most two claimed items and processes them in claim order; every wait of
-// an item refers to items with smaller indices, held by running CTAs, so the
-// grid always progresses.  A CTA claims item k+2 only while item k+1 exists,
-// so every CTA makes exactly one claim beyond the end of the list.
-template <int S, int OPS, bool BULK, bool ALIGN>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
-{
-    __shared__ ItemShared sh[2];
-    __shared__ Slot slot[2];
-    __shared__ int s_ok;
-    extern __shared__ __align__(128) char dyn[];
-    BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u};
-    const int tid = (int)threadIdx.x;
-    if (tid == 0) {
-        if (BULK) {
-            for (int i = 0; i < stages; ++i)
-                mbar_init(&bk.bar[i], 1u);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        const unsigned i0 = claim(a, 0);
-        const unsigned i1 = i0 < a.nitems ? claim(a, 1) : ~0u;
-        // both header loads in flight before either is stored
-        Item h0{}, h1{};
-        if (i0 < a.nitems)
-            h0 = a.items[i0];
-        if (i1 < a.nitems)
-            h1 = a.items[i1];
-        slot[0].index = i0;
-        slot[1].index = i1;
-        slot[0].item = h0;
-        slot[1].item = h1;
-    }
-    __syncthreads();
-    if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
-        put_ref<S>(a, slot[0].item, a.refs[slot[0].item.ref + tid], sh[0], tid);
-    __syncthreads();
-
-    for (unsigned k = 0;; ++k) {
-        const int cur = (int)(k & 1u), nxt = cur ^ 1;
-        const unsigned index = slot[cur].index;
-        if (index >= a.nitems)
-            break;
-        const Item it = slot[cur].item;
-        const unsigned next_index = slot[nxt].index;
-        // This thread's reference of item k+1: loaded now, stored after the move.
-        const Item nit = slot[nxt].item;
-        const bool has_ref = next_index < a.nitems && tid < nit.nsrc + nit.ndst;
-        Ref nref{};
-        if (has_ref)
-            nref = a.refs[nit.ref + tid];
-        unsigned i2 = ~0u;
-        Item h2{};
-        if (tid == 0 && next_index < a.nitems) {
-            i2 = claim(a, k + 2);
-            if (i2 < a.nitems)
-                h2 = a.items[i2];
-        }
-        if (tid < 32) {
-            const bool ok = it.nwait ? run_waits(a, it, tid) : true;
-            if (tid == 0)
-                s_ok = ok ? 1 : 0;
-        }
-        __syncthreads();
-        if (s_ok)
-            move_item<S, OPS, BULK, ALIGN>(sh[cur], it.nsrc, it.ndst, it.rows, it.cols, bk, a);
-        if (has_ref)
-            put_ref<S>(a, nit, nref, sh[nxt], tid);  // sh[nxt] served item k-1, done before the last barrier
-        if (tid == 0) {
-            // every thread read slot[cur] and slot[nxt] before the barrier above
-            slot[cur].index = i2;
-            slot[cur].item = h2;
-        }
-        __syncthreads();
-        if (tid < 32 && s_ok && it.npost)
-            run_posts(a, it, index, tid);
-    }
-
-    if (a.use_tickets && tid == 0) {
-        __threadfence();
-        if (atomicAdd(a.st.exited, 1u) == gridDim.x - 1) {
-            // Last CTA out: every other CTA has taken its final ticket.
-            *a.st.ticket = 0u;
-            *a.st.exited = 0u;
-            __threadfence();
-        }
-    }
-}
-
-}  // namespace
-
-namespace {
-
-template <int S, int OPS, bool BULK, bool ALIGN>
-cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
-{
-    size_t dyn = BULK ? 128 + (size_t)stages * kBulkPiece : 0;
-    if (BULK) {
-        static bool configured = false;  // per instantiation; the attribute is per function
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(snac_kernel<S, OPS, BULK, ALIGN>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)(128 + (size_t)kBulkMaxStages * kBulkPiece));
-            if (e != cudaSuccess)
-                return e;
-            configured = true;
-        }
-    }
-    snac_kernel<S, OPS, BULK, ALIGN><<<ctas, kThreads, dyn, stream>>>(args, stages);
-    return cudaGetLastError();
-}
-
-template <int S, bool BULK, bool ALIGN>
-cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
-{
-    if (args.ops == kOpsCopy)
-        return launch_one<S, kOpsCopy, BULK, ALIGN>(args, ctas, stages, stream);
-    if (args.ops == kOpsSum)
-        return launch_one<S, kOpsSum, false, ALIGN>(args, ctas, stages, stream);
-    if (args.ops == (kOpsSum | kOpsWide))
-        return launch_one<S, kOpsSum | kOpsWide, false, ALIGN>(args, ctas, stages, stream);
-    return launch_one<S, kOpsCopy | kOpsSum, BULK, ALIGN>(args, ctas, stages, stream);
-}
-
-template <int S>
-cudaError_t launch_dtype(const LaunchArgs& args, int ctas, bool bulk, bool aligned, int stages, cudaStream_t stream)
-{
-    if (bulk)
-        return aligned ? launch_ops<S, true, true>(args, ctas, stages, stream)
-                       : launch_ops<S, true, false>(args, ctas, stages, stream);
-    return aligned ? launch_ops<S, false, true>(args, ctas, stages, stream)
-                   : launch_ops<S, false, false>(args, ctas, stages, stream);
-}
-
-}  // namespace
 
 cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream)
 {
@@ -950,9 +20,18 @@ cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages,
     bool aligned = args.all_aligned != 0;
     for (int i = 0; aligned && i < args.nbufs; ++i)
         aligned = (reinterpret_cast<uintptr_t>(args.bufs[i]) & 15u) == 0;
-    if (args.dtype == 0)
-        return launch_dtype<2>(args, ctas, bulk, aligned, stages, stream);
-    return launch_dtype<4>(args, ctas, bulk, aligned, stages, stream);
+    switch (args.dtype) {
+    case kDtBf16:
+        return launch_snac_bf16(args, ctas, bulk, aligned, stages, stream);
+    case kDtFp32:
+        return launch_snac_fp32(args, ctas, bulk, aligned, stages, stream);
+    case kDtFp16:
+        return launch_snac_fp16(args, ctas, bulk, aligned, stages, stream);
+    case kDtFp8:
+        return launch_snac_fp8(args, ctas, bulk, aligned, stages, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 int snac_ctas_per_sm(bool bulk, int stages)
@@ -960,7 +39,8 @@ int snac_ctas_per_sm(bool bulk, int stages)
     (void)bulk;
     (void)stages;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<2, kOpsCopy | kOpsSum, false, false>, kThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, false>,
+                                                      kThreads, 0) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

@@ -1,0 +1,12 @@
+// The one-byte (fp8) instantiation of the persistent SNAC kernel: copies only
+// (see atom_impl.cuh).
+#include "atom_impl.cuh"
+
+namespace purlin {
+
+cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s)
+{
+    return launch_dtype<kDtFp8>(a, ctas, bulk, aligned, stages, s);
+}
+
+}  // namespace purlin

@@ -79,11 +79,11 @@ pl_status setup_device(int dev, DeviceSetup*& out)
 extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t count, void* const* in_bufs,
                                                  void* const* out_bufs, int wait, void* stream)
 {
-    if (R < 1 || !in_bufs || !out_bufs || (dtype != PL_BF16 && dtype != PL_FP32))
+    if (R < 1 || !in_bufs || !out_bufs || (dtype != PL_BF16 && dtype != PL_FP32 && dtype != PL_FP16))
         return PL_ERR_INVALID;
     if (R > kMaxRanksNoAlloc)
         return PL_ERR_NOMEM;  // the work list of more ranks may not fit the array
-    const uint64_t esize = dtype == PL_BF16 ? 2 : 4;
+    const uint64_t esize = dtype == PL_FP32 ? 4 : 2;
     if (count > kMaxBytesPerRank / esize)
         return PL_ERR_NOMEM;  // beyond what the static array is sized for
     if (count == 0)

@@ -41,7 +41,29 @@ constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threa
 constexpr size_t kMaxCachedPlans = 1024;
 constexpr uint32_t kMaxUsesPerLaunch = (1u << 24) - 2;
 
-uint64_t elem_size(pl_dtype dt) { return dt == PL_BF16 ? 2 : 4; }
+uint64_t elem_size(pl_dtype dt)
+{
+    switch (dt) {
+    case PL_BF16:
+    case PL_FP16:
+        return 2;
+    case PL_FP8:
+        return 1;
+    default:
+        return 4;
+    }
+}
+
+// PL_OK for a known op and dtype the datapath can run; one-byte elements are
+// moved, never reduced.
+pl_status check_op_dtype(pl_op op, pl_dtype dt)
+{
+    if ((op != PL_COPY && op != PL_SUM && op != PL_MAX) || dt < PL_BF16 || dt > PL_FP8)
+        return PL_ERR_INVALID;
+    if (dt == PL_FP8 && op != PL_COPY)
+        return PL_ERR_UNSUPPORTED;
+    return PL_OK;
+}
 
 }  // namespace
 
@@ -352,7 +374,7 @@ struct HostPlan {
     std::vector<Sync> syncs;
     uint32_t nflags = 0;
     int lag = 0;          // chunk rows between producers and their consumers in claim order
-    int ops = 0;          // kOpsCopy | kOpsSum
+    int ops = 0;          // kOpsCopy | kOpsReduce, plus kOpsWide / kOpsMax
     int all_aligned = 0;  // every reference's byte offset and row stride is a multiple of 16
     pl_plan_stats stats{};
 };
@@ -512,7 +534,7 @@ public:
     {
         Item it{};
         it.kind = kind;
-        it.op = (uint8_t)(op == PL_SUM && p.src.size() > 1 ? 1 : 0);
+        it.op = (uint8_t)(op != PL_COPY && p.src.size() > 1 ? (op == PL_MAX ? 2 : 1) : 0);
         it.nsrc = (uint16_t)p.src.size();
         it.ndst = (uint16_t)p.dst.size();
         it.rows = (uint32_t)c.nrows;
@@ -623,7 +645,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     // bytes resident in L2, so consumers read them from there.
     bool multi_dst_sum = false;
     for (const Transfer& t : ts)
-        multi_dst_sum |= op == PL_SUM && t.srcs.size() > 1 && t.dsts.size() > 1;
+        multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
     const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
     if (ticketed && pol.chunk_bytes == 0)
         chunk_bytes = std::min<uint64_t>(chunk_bytes, kTicketedChunkBytes);
@@ -703,7 +725,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
             const Transfer& t = ts[ti];
             const Chunk& ch = chunks[ti][c];
             const uint64_t blk = ch.nrows * ch.ncols * S;
-            const bool sum = op == PL_SUM && t.srcs.size() > 1;
+            const bool sum = op != PL_COPY && t.srcs.size() > 1;  // a reduction (sum or maximum)
 
             if (!staged) {
                 if (sum && t.dsts.size() > 1 && pol.ar_form == PL_AR_COMPOSED) {
@@ -870,7 +892,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
             wide &= it.nsrc >= 8;
         if (it.nsrc > kMaxRanks || it.ndst > kMaxRanks || it.nsrc == 0 || it.ndst == 0)
             return PL_ERR_UNSUPPORTED;  // the kernel holds at most 64 sources and 64 destinations
-        hp.ops |= it.op ? kOpsSum : kOpsCopy;
+        hp.ops |= it.op ? kOpsReduce : kOpsCopy;
         for (uint32_t k = it.ref; k < it.ref + it.nsrc + it.ndst; ++k) {
             const Ref& f = hp.refs[k];
             if ((f.offset * S) % 16 || (it.rows > 1 && (f.stride * S) % 16))
@@ -879,8 +901,11 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     }
     // bf16 sums of 8+ sources stream best as 1 vector x 8 sources per step;
     // fp32 sums and fewer sources as 2 vectors x 4 sources (measured on GB300).
-    if (hp.ops == kOpsSum && wide && dt == PL_BF16)
+    // fp16 has bf16's vector shape and takes its rule.
+    if (hp.ops == kOpsReduce && wide && op == PL_SUM && (dt == PL_BF16 || dt == PL_FP16))
         hp.ops |= kOpsWide;
+    if (op == PL_MAX && (hp.ops & kOpsReduce))
+        hp.ops |= kOpsMax;
     if (tickets && !waits_precede(hp))
         return PL_ERR_NOMEM;
 
@@ -941,8 +966,9 @@ PL_API pl_status pl_plan_create(pl_plan** plan, const pl_layout* in, const pl_la
 {
     if (!plan || !in || !out || R < 1 || R > kMaxRanks || num_sms < 1)
         return PL_ERR_INVALID;
-    if ((op != PL_COPY && op != PL_SUM) || (dtype != PL_BF16 && dtype != PL_FP32))
-        return PL_ERR_INVALID;
+    pl_status vs = check_op_dtype(op, dtype);
+    if (vs != PL_OK)
+        return vs;
     ResolvedPolicy rp;
     pl_status st = resolve_policy(policy, rp);
     if (st != PL_OK)
@@ -1347,10 +1373,11 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         return PL_ERR_INVALID;
     if (R < 1 || R > kMaxRanks || in->R != R || out->R != R)
         return PL_ERR_INVALID;
-    if ((op != PL_COPY && op != PL_SUM) || (dt != PL_BF16 && dt != PL_FP32))
-        return PL_ERR_INVALID;
+    pl_status st = check_op_dtype(op, dt);
+    if (st != PL_OK)
+        return st;
     ResolvedPolicy rp;
-    pl_status st = resolve_policy(policy, rp);
+    st = resolve_policy(policy, rp);
     if (st != PL_OK)
         return st;
     if ((st = check_buffers(*in, *out, dt, R, in_bufs, in_counts, out_bufs, out_counts)) != PL_OK)
@@ -1404,10 +1431,10 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     return PL_OK;
 }
 
-PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dt, int R, uint64_t count, void* const* in_bufs,
-                              void* const* out_bufs, const pl_policy* policy, void* stream)
+PL_API pl_status pl_allreduce_op(pl_ctx* ctx, pl_op op, pl_dtype dt, int R, uint64_t count, void* const* in_bufs,
+                                 void* const* out_bufs, const pl_policy* policy, void* stream)
 {
-    if (!ctx || R < 1 || R > kMaxRanks)
+    if (!ctx || R < 1 || R > kMaxRanks || op == PL_COPY)
         return PL_ERR_INVALID;
     auto key = std::make_pair(R, count);
     auto it = ctx->ar_layouts.find(key);
@@ -1421,8 +1448,14 @@ PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dt, int R, uint64_t count, v
         it = ctx->ar_layouts.emplace(key, L).first;
     }
     std::vector<uint64_t> counts(R, count);
-    return pl_collective(ctx, it->second, it->second, PL_SUM, dt, R, in_bufs, counts.data(), out_bufs,
+    return pl_collective(ctx, it->second, it->second, op, dt, R, in_bufs, counts.data(), out_bufs,
                          counts.data(), policy, stream);
+}
+
+PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dt, int R, uint64_t count, void* const* in_bufs,
+                              void* const* out_bufs, const pl_policy* policy, void* stream)
+{
+    return pl_allreduce_op(ctx, PL_SUM, dt, R, count, in_bufs, out_bufs, policy, stream);
 }
 
 }  // extern "C"
@@ -1434,7 +1467,7 @@ namespace purlin {
 int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bufs, void* const* out_bufs,
                             int num_sms, uint64_t ring_bytes, uint64_t chunk_bytes, HostWorkList& out)
 {
-    if (R < 1 || R > kMaxRanks || !in_bufs || !out_bufs || (dtype != PL_BF16 && dtype != PL_FP32))
+    if (R < 1 || R > kMaxRanks || !in_bufs || !out_bufs || (dtype != PL_BF16 && dtype != PL_FP32 && dtype != PL_FP16))
         return PL_ERR_INVALID;
     std::vector<uint64_t> lens(R, count / (uint64_t)R);
     lens[R - 1] = count - (count / (uint64_t)R) * (uint64_t)(R - 1);

@@ -1,6 +1,6 @@
 // Internal layout of a SNAC work list as the device reads it, and the launch
 // interface between the host runtime (runtime.cpp) and the Atom kernels
-// (atom.cu).  Not part of the public ABI.
+// (atom_impl.cuh and its per-dtype instantiations).  Not part of the public ABI.
 #pragma once
 
 #include <cstdint>
@@ -18,19 +18,26 @@ constexpr int kBulkMaxStages = 8;
 enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2 };
 enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3 };
 
+// Element types of a launch (the same codes as the public pl_dtype values).
+constexpr int kDtBf16 = 0;
+constexpr int kDtFp32 = 1;
+constexpr int kDtFp16 = 2;
+constexpr int kDtFp8 = 3;  // any one-byte element: copied, never reduced
+
 // Which moves a work list contains: the kernel is instantiated per mix so that
-// a copy-only or sum-only list gets code without the other path.
+// a copy-only or reduce-only list gets code without the other path.
 constexpr int kOpsCopy = 1;
-constexpr int kOpsSum = 2;
-constexpr int kOpsWide = 4;  // every sum has at least 8 sources: one vector x 8 sources per step
+constexpr int kOpsReduce = 2;  // items with several sources reduce them
+constexpr int kOpsWide = 4;    // every sum has at least 8 sources: one vector x 8 sources per step
+constexpr int kOpsMax = 8;     // the reduction is the maximum, not the sum
 
 // One work item: move a rows x cols block from nsrc sources (copy if nsrc == 1,
-// rank-ordered fp32 sum otherwise) into ndst destinations.  Refs
+// rank-ordered reduction otherwise) into ndst destinations.  Refs
 // [ref, ref + nsrc) are sources, [ref + nsrc, ref + nsrc + ndst) destinations.
 // Syncs [sync, sync + nwait) run before the move, [sync + nwait, + npost) after.
 struct Item {
     uint8_t kind;
-    uint8_t op;        // 0 copy, 1 sum
+    uint8_t op;        // 0 copy, 1 sum, 2 maximum
     uint16_t nsrc;
     uint16_t ndst;
     uint16_t nwait;
@@ -80,9 +87,9 @@ struct LaunchArgs {
     const Sync* syncs;
     uint32_t nitems;
     int32_t use_tickets;
-    int32_t dtype;               // 0 bf16, 1 fp32
+    int32_t dtype;               // kDtBf16, kDtFp32, kDtFp16 or kDtFp8
     int32_t nbufs;
-    int32_t ops;                 // kOpsCopy | kOpsSum present in the list
+    int32_t ops;                 // kOpsCopy | kOpsReduce present in the list, plus kOpsWide / kOpsMax
     int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
     unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
     unsigned long long timeout_ns;
@@ -94,6 +101,14 @@ struct LaunchArgs {
 // Launch of the persistent SNAC kernel (atom.cu).  `bulk` selects the
 // cp.async.bulk shared-memory ring for copy items with `stages` stages.
 cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream);
+
+// The per-element-type launchers behind launch_snac (atom.cu, atom_fp16.cu,
+// atom_fp32.cu, atom_fp8.cu).  `aligned`: every reference and buffer is
+// 16-byte aligned, so the kernels without realigning bodies serve the plan.
+cudaError_t launch_snac_bf16(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
+cudaError_t launch_snac_fp16(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
+cudaError_t launch_snac_fp32(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
+cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
 
 // CTAs of the SNAC kernel that fit on one SM at once.
 int snac_ctas_per_sm(bool bulk, int stages);

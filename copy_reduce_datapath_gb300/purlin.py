@@ -21,8 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libpurlin1.so")
 
 PL_OK, PL_ERR_INVALID, PL_ERR_LAYOUT, PL_ERR_ALIAS = 0, 1, 2, 3
 PL_ERR_NOMEM, PL_ERR_CUDA, PL_ERR_TIMEOUT, PL_ERR_UNSUPPORTED = 4, 5, 6, 7
-PL_COPY, PL_SUM = 0, 1
-PL_BF16, PL_FP32 = 0, 1
+PL_COPY, PL_SUM, PL_MAX = 0, 1, 2
+PL_BF16, PL_FP32, PL_FP16, PL_FP8 = 0, 1, 2, 3
 PL_PATH_AUTO, PL_PATH_ZS, PL_PATH_STAGED = 0, 1, 2
 PL_AR_AUTO, PL_AR_FUSED, PL_AR_COMPOSED = 0, 1, 2
 PL_ATOM_AUTO, PL_ATOM_VECTOR, PL_ATOM_BULK = 0, 1, 2
@@ -30,8 +30,8 @@ PL_ITEM_MOVE, PL_ITEM_STAGE, PL_ITEM_CONSUME = 0, 1, 2
 PL_SPACE_IN, PL_SPACE_OUT, PL_SPACE_SCRATCH = 0, 1, 2
 PL_SYNC_WAIT_FULL, PL_SYNC_WAIT_FREE, PL_SYNC_NOTIFY, PL_SYNC_CREDIT = 0, 1, 2, 3
 
-DTYPES = {"bf16": PL_BF16, "fp32": PL_FP32}
-OPS = {"copy": PL_COPY, "sum": PL_SUM}
+DTYPES = {"bf16": PL_BF16, "fp32": PL_FP32, "fp16": PL_FP16, "fp8": PL_FP8}
+OPS = {"copy": PL_COPY, "sum": PL_SUM, "max": PL_MAX}
 
 
 class PurlinError(RuntimeError):
@@ -102,6 +102,7 @@ def _load():
         "pl_collective": (i32, [vp, vp, vp, i32, i32, C.c_int, vpp, u64p, vpp, u64p,
                                 C.POINTER(pl_policy), vp]),
         "pl_allreduce": (i32, [vp, i32, C.c_int, u64, vpp, vpp, C.POINTER(pl_policy), vp]),
+        "pl_allreduce_op": (i32, [vp, i32, i32, C.c_int, u64, vpp, vpp, C.POINTER(pl_policy), vp]),
         "pl_allreduce_noalloc": (i32, [i32, C.c_int, u64, vpp, vpp, C.c_int, vp]),
         "pl_plan_create": (i32, [vpp, vp, vp, i32, i32, C.c_int, C.POINTER(pl_policy), C.c_int, u64]),
         "pl_plan_destroy": (i32, [vp]),
@@ -276,6 +277,13 @@ def pl_allreduce(ctx, dtype, R, count, in_ptrs, out_ptrs, policy: pl_policy | No
     st = lib.pl_allreduce(ctx, _dtype(dtype), R, count, _ptrs(in_ptrs), _ptrs(out_ptrs),
                           C.byref(policy) if policy is not None else None, stream or None)
     _check(st, "pl_allreduce")
+
+
+def pl_allreduce_op(ctx, op, dtype, R, count, in_ptrs, out_ptrs, policy: pl_policy | None = None,
+                    stream: int = 0) -> None:
+    st = lib.pl_allreduce_op(ctx, _op(op), _dtype(dtype), R, count, _ptrs(in_ptrs), _ptrs(out_ptrs),
+                             C.byref(policy) if policy is not None else None, stream or None)
+    _check(st, "pl_allreduce_op")
 
 
 def pl_allreduce_noalloc(dtype, R, count, in_ptrs, out_ptrs, wait: bool = True, stream: int = 0) -> int:

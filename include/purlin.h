@@ -65,16 +65,23 @@ typedef int32_t pl_status;
 #define PL_ERR_NOMEM        4 /* device allocation failed, or the scratch ring is too small for the staged path */
 #define PL_ERR_CUDA         5 /* a CUDA call failed; pl_ctx_cuda_error() returns the cudaError_t value */
 #define PL_ERR_TIMEOUT      6 /* a bounded device wait expired (reported by pl_ctx_status) */
-#define PL_ERR_UNSUPPORTED  7 /* a valid layout pair this datapath does not handle (two strided regions of one
-                                 transfer with different row lengths) */
+#define PL_ERR_UNSUPPORTED  7 /* a valid request this datapath does not handle: two strided regions of one
+                                 transfer with different row lengths, or a reduction of PL_FP8 elements */
 
 typedef int32_t pl_op;
 #define PL_COPY 0 /* every output region receives the unique input region of the same name */
 #define PL_SUM  1 /* every output region receives the rank-ordered sum of the R input regions of its name */
+#define PL_MAX  2 /* every output region receives the rank-ordered maximum of the R input regions of its name:
+                     start from rank 0's element and take rank r's when it compares greater (so a NaN counts
+                     only from rank 0, and of +0 and -0 the lower rank's is kept).  Not in the pages, whose
+                     reductions are sums; it uses the same layouts and work lists. */
 
 typedef int32_t pl_dtype;
 #define PL_BF16 0 /* bfloat16 in and out; sums accumulate in fp32 and round once (nearest-even) */
 #define PL_FP32 1 /* float32 in and out; sums accumulate in fp32 */
+#define PL_FP16 2 /* IEEE binary16 in and out; sums accumulate in fp32 and round once (nearest-even) */
+#define PL_FP8  3 /* any one-byte element (e4m3, e5m2, bytes): PL_COPY only; PL_SUM / PL_MAX give
+                     PL_ERR_UNSUPPORTED.  Every layout offset and length is then a byte count. */
 
 /* --------------------------------------------------------------- policies */
 
@@ -220,6 +227,13 @@ PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dtype, int R, uint64_t count
                               void* const* in_bufs, void* const* out_bufs,
                               const pl_policy* policy, void* stream);
 
+/* pl_allreduce with the reduction named: op = PL_SUM (the same call) or
+ * PL_MAX (out_bufs[r][i] = rank-ordered maximum over ranks of in_bufs[*][i]).
+ * PL_COPY returns PL_ERR_INVALID; PL_FP8 returns PL_ERR_UNSUPPORTED. */
+PL_API pl_status pl_allreduce_op(pl_ctx* ctx, pl_op op, pl_dtype dtype, int R, uint64_t count,
+                                 void* const* in_bufs, void* const* out_bufs,
+                                 const pl_policy* policy, void* stream);
+
 /* AllReduce that allocates no device memory.  The paper has no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- a process
  * that reserves its device memory budget once at start-up and may not grow it,
@@ -227,7 +241,8 @@ PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dtype, int R, uint64_t count
  * latency path where an allocation (which can synchronise the device) is not
  * acceptable.  The result is the same as pl_allreduce with a staged policy:
  * out_bufs[r][i] = rank-ordered fp32 sum over ranks of in_bufs[*][i], rounded
- * once to dtype, for every r (out_bufs may equal in_bufs).
+ * once to dtype, for every r (out_bufs may equal in_bufs).  dtype is
+ * PL_BF16, PL_FP16 or PL_FP32.
  *
  * No context: the flag words, the derived work list and the staging ring live
  * in one file-scope device array of 32 MiB that every GPU loading the library

@@ -54,7 +54,7 @@ def _np_dtype(dtype: str):
     try:
         return _DT[dtype]
     except KeyError:
-        raise ValueError(f"oracle dtype must be 'bf16' or 'fp32', not {dtype!r}") from None
+        raise ValueError(f"oracle dtype must be one of {sorted(_DT)}, not {dtype!r}") from None
 
 
 def _ptrs(arrs):

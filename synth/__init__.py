@@ -104,9 +104,13 @@ def host_tensor(kind: str, dtype: str, seed: int, rank: int, n: int):
     """A 1-D torch CPU tensor of ``n`` elements for logical rank ``rank``.
 
     kind: "normal" (N(0,1)), "uniform" (U(-1,1)) or "int8range" (integers in [-8, 8]).
-    dtype: "bf16" or "fp32".
+    dtype: "bf16", "fp16" (PyTorch's round-to-nearest-even casts of the fp32 draw),
+    "fp32", or "fp8": one-byte elements, for which ``kind`` is ignored and every
+    byte is drawn uniformly from the SplitMix64 stream (all 256 patterns occur).
     """
     import torch
+    if dtype == "fp8":
+        return torch.from_numpy(random_bytes(seed, rank, n))
     if kind == "normal":
         a = normal_f32(seed, rank, n)
     elif kind == "uniform":
@@ -117,9 +121,16 @@ def host_tensor(kind: str, dtype: str, seed: int, rank: int, n: int):
         raise ValueError(f"unknown input kind {kind!r}")
     if dtype == "bf16":
         return to_bf16(a)
+    if dtype == "fp16":
+        return torch.from_numpy(a).to(torch.float16)
     if dtype == "fp32":
         return torch.from_numpy(a)
     raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def random_bytes(seed: int, rank: int, n: int) -> np.ndarray:
+    """n bytes, the top byte of each SplitMix64 output of stream (seed, rank)."""
+    return (u64_stream(seed, rank, n) >> np.uint64(56)).astype(np.uint8)
 
 
 def zipf_lengths(total: int, R: int, s: float, seed: int, stream: int = 0) -> list[int]:
@@ -195,3 +206,11 @@ def device_uniform_pm1(seed: int, rank: int, n: int, device, dtype):
         e = min(n, s + step)
         out[s:e] = (torch.rand(e - s, generator=g, device=device, dtype=torch.float32) * 2 - 1).to(dtype)
     return out
+
+
+def device_bytes(seed: int, rank: int, n: int, device):
+    """Uniform bytes drawn on ``device`` by PyTorch's seeded generator (large one-byte inputs)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(device_seed(seed, rank))
+    return torch.randint(0, 256, (n,), generator=g, device=device, dtype=torch.uint8)

@@ -23,13 +23,20 @@ from copy_reduce_datapath_gb300 import purlin as P
 def _to_f32(dtype, a):
     if dtype == "fp32":
         return a.astype(np.float32)
+    if dtype == "fp16":
+        return np.ascontiguousarray(a, np.uint16).view(np.float16).astype(np.float32)
     return (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
 def _from_f32(dtype, a):
     if dtype == "fp32":
         return a.astype(np.float32)
+    if dtype == "fp16":
+        return np.ascontiguousarray(a, np.float32).astype(np.float16).view(np.uint16)
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+NPDT = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "fp8": np.uint8}
 
 
 class Stall(AssertionError):
@@ -51,7 +58,7 @@ def _index(ref, rows, cols):
 def run(plan, R, dtype, ins, outs, *, window=1, seed=0):
     """Execute `plan` over numpy buffers `ins`/`outs` (modified in place)."""
     st, items = load_plan(plan)
-    npdt = np.uint16 if dtype == "bf16" else np.float32
+    npdt = NPDT[dtype]
     scratch = np.zeros(max(1, R * st.slots * st.slot_elems), dtype=npdt)
     space = {P.PL_SPACE_IN: ins, P.PL_SPACE_OUT: outs, P.PL_SPACE_SCRATCH: [scratch]}
     full = defaultdict(int)
@@ -75,9 +82,14 @@ def run(plan, R, dtype, ins, outs, *, window=1, seed=0):
             vals.append(buf[_index(ref, it.rows, it.cols)].copy())
         if it.nsrc == 1:
             return vals[0]
+        assert dtype != "fp8", "a reduction of one-byte elements"
         acc = _to_f32(dtype, vals[0])
         for v in vals[1:]:
-            acc = (acc + _to_f32(dtype, v)).astype(np.float32)
+            x = _to_f32(dtype, v)
+            if it.op == 2:  # maximum: the later rank's value only when greater
+                acc = np.where(x > acc, x, acc).astype(np.float32)
+            else:
+                acc = (acc + x).astype(np.float32)
         return _from_f32(dtype, acc)
 
     def write(it, refs, data):

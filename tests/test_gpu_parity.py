@@ -9,13 +9,11 @@ import oracle
 import synth
 from copy_reduce_datapath_gb300 import purlin as P
 
-from gpu_util import NP, TORCH, assert_equal, empty, host, to_dev, to_np
+from gpu_util import NP, TORCH, Outs, ar_policies, assert_equal, empty, host, policies, run, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
 SCRATCH = 64 << 20
-CANARY = {"bf16": 0x7FA5, "fp32": 0x7FA5A5A5}  # NaN patterns no collective produces here
-GUARD = 37  # elements of canary before and after every output
 
 
 @pytest.fixture(scope="module")
@@ -24,61 +22,6 @@ def ctx():
     c = P.pl_ctx_create(0, SCRATCH)
     yield c
     P.pl_ctx_destroy(c)
-
-
-def policies():
-    return {
-        "zs": P.pl_policy_default(),
-        "zs_small_chunks": P.pl_policy_default(chunk_bytes=4096),
-        "staged": P.pl_policy_default(path=P.PL_PATH_STAGED, chunk_bytes=8192),
-    }
-
-
-def ar_policies():
-    return {
-        "zs_fused": P.pl_policy_default(),
-        "zs_composed": P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=8192),
-        "staged_fused": P.pl_policy_default(path=P.PL_PATH_STAGED, chunk_bytes=8192),
-        "staged_composed": P.pl_policy_default(path=P.PL_PATH_STAGED, allreduce_form=P.PL_AR_COMPOSED,
-                                               chunk_bytes=8192),
-    }
-
-
-class Outs:
-    """Output buffers with canary guard regions on both sides."""
-
-    def __init__(self, sizes, dtype):
-        self.dtype = dtype
-        self.sizes = [int(s) for s in sizes]
-        self.full = [empty(s + 2 * GUARD, dtype, fill=CANARY[dtype]) for s in self.sizes]
-        self.views = [f[GUARD:GUARD + s] for f, s in zip(self.full, self.sizes)]
-
-    def ptrs(self):
-        return P.ptrs(self.views)
-
-    def counts(self):
-        return self.sizes
-
-    def host(self, r):
-        return to_np(self.views[r], self.dtype)
-
-    def check_guards(self):
-        for r, f in enumerate(self.full):
-            a = to_np(f, self.dtype)
-            bits = a.view(np.uint16 if self.dtype == "bf16" else np.uint32)
-            assert np.all(bits[:GUARD] == CANARY[self.dtype]), f"rank {r}: write before its output"
-            assert np.all(bits[GUARD + self.sizes[r]:] == CANARY[self.dtype]), f"rank {r}: write past its output"
-
-
-def run(ctx, lin, lout, op, dtype, ins_host, out_sizes, pol):
-    R = len(ins_host)
-    ins = [to_dev(a, dtype) for a in ins_host]
-    outs = Outs(out_sizes, dtype)
-    s = P.stream_handle()
-    P.pl_collective(ctx, lin, lout, op, dtype, R, P.ptrs(ins), P.counts(ins), outs.ptrs(), outs.counts(), pol, s)
-    assert P.pl_ctx_status(ctx, s) == P.PL_OK
-    outs.check_guards()
-    return [outs.host(r) for r in range(R)]
 
 
 # ------------------------------------------------------- the five workloads

@@ -9,12 +9,12 @@ from copy_reduce_datapath_gb300 import purlin as P
 
 import plan_interp
 
-NP = {"bf16": np.uint16, "fp32": np.float32}
+NP = plan_interp.NPDT
 
 
 def rand(dtype, seed, rank, n):
     t = synth.host_tensor("normal", dtype, seed, rank, n)
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp16"):
         import torch
         return t.view(torch.int16).numpy().view(np.uint16).copy()
     return t.numpy().copy()
@@ -39,7 +39,7 @@ def run_and_check(plan, R, dtype, ins, outs, want, window, seed=0):
         assert np.array_equal(outs[r], want[r]), f"rank {r}"
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "fp16", "fp8"])
 @pytest.mark.parametrize("path,scratch", PATHS)
 @pytest.mark.parametrize("window", WINDOWS)
 def test_allgather_v(dtype, path, scratch, window):
@@ -53,17 +53,18 @@ def test_allgather_v(dtype, path, scratch, window):
     run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("fp32", "sum"), ("fp16", "sum"), ("bf16", "max"),
+                                      ("fp16", "max")])
 @pytest.mark.parametrize("path,scratch", PATHS)
 @pytest.mark.parametrize("window", WINDOWS)
-def test_reducescatter_v(dtype, path, scratch, window):
+def test_reducescatter_v(dtype, op, path, scratch, window):
     R = 4
     lens = [100, 3, 0, 250]
     N = sum(lens)
     ins = [rand(dtype, 2, r, N) for r in range(R)]
-    want = oracle.reducescatter(ins, lens, dtype)
+    want = oracle.reducescatter(ins, lens, dtype, op=op)
     lin, lout = P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens)
-    pl = plan_for(lin, lout, "sum", dtype, R, policy(path), scratch)
+    pl = plan_for(lin, lout, op, dtype, R, policy(path), scratch)
     outs = [np.zeros(lens[k], NP[dtype]) for k in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
 
@@ -85,23 +86,24 @@ def test_reducescatter_in_place(path, scratch):
         o += lens[k]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("fp32", "sum"), ("fp16", "sum"), ("fp32", "max"),
+                                      ("bf16", "max")])
 @pytest.mark.parametrize("path,scratch", PATHS)
 @pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
 @pytest.mark.parametrize("window", WINDOWS)
-def test_allreduce(dtype, path, scratch, form, window):
+def test_allreduce(dtype, op, path, scratch, form, window):
     R = 3
     N = 3 * 301
     ins = [rand(dtype, 4, r, N) for r in range(R)]
-    want = oracle.allreduce(ins, dtype)
+    want = oracle.allreduce(ins, dtype, op=op)
     lens = synth.equal_lengths(N, R)
     L = P.pl_layout_partitioned(R, lens)
-    pl = plan_for(L, L, "sum", dtype, R, policy(path, form), scratch)
+    pl = plan_for(L, L, op, dtype, R, policy(path, form), scratch)
     outs = [np.zeros(N, NP[dtype]) for _ in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window, seed=window)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "fp8"])
 @pytest.mark.parametrize("path,scratch", PATHS)
 @pytest.mark.parametrize("window", WINDOWS)
 def test_alltoall_v(dtype, path, scratch, window):
@@ -212,3 +214,40 @@ def test_staged_needs_a_ring():
     with pytest.raises(P.PurlinError) as e:
         plan_for(L, L, "sum", "bf16", R, policy(P.PL_PATH_STAGED, chunk=1024), scratch=R * 1024)
     assert e.value.status == P.PL_ERR_NOMEM
+
+
+def test_op_and_dtype_codes_are_checked():
+    """One-byte elements are moved, never reduced; unknown codes are invalid."""
+    R = 2
+    L = P.pl_layout_partitioned(R, [8, 8])
+    for op in ("sum", "max"):
+        with pytest.raises(P.PurlinError) as e:
+            plan_for(L, L, op, "fp8", R, None)
+        assert e.value.status == P.PL_ERR_UNSUPPORTED
+    plan_for(P.pl_layout_rank_owned(R, [8, 8]), L, "copy", "fp8", R, None)
+    for op, dt in ((3, "bf16"), (-1, "bf16"), ("sum", 4), ("copy", -1)):
+        with pytest.raises(P.PurlinError) as e:
+            plan_for(L, L, op, dt, R, None)
+        assert e.value.status == P.PL_ERR_INVALID
+
+
+def test_reduction_items_name_their_op():
+    """Work items that reduce carry the op (1 sum, 2 maximum); copies carry 0."""
+    R = 4
+    L = P.pl_layout_partitioned(R, [64] * R)
+    for op, code in (("sum", 1), ("max", 2)):
+        pl = plan_for(L, L, op, "bf16", R, policy(P.PL_PATH_ZS, P.PL_AR_COMPOSED))
+        ops = {P.pl_plan_get_item(pl, i)[0].op for i in range(P.pl_plan_get_stats(pl).items)}
+        assert ops == {0, code}
+
+
+def test_one_byte_chunks_and_alignment():
+    """Chunks of one-byte elements are whole 16-byte vectors; a plan whose
+    byte offsets are all multiples of 16 covers every element exactly once."""
+    R = 8
+    lens = [4096 + 16 * r for r in range(R)]
+    pl = plan_for(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy", "fp8", R,
+                  policy(P.PL_PATH_ZS, chunk=1024))
+    st = P.pl_plan_get_stats(pl)
+    assert st.chunk_elems % 16 == 0
+    assert st.bytes_read == sum(lens) and st.bytes_written == R * sum(lens)
