@@ -60,6 +60,8 @@ def parse():
                     help="Atom copy of 256 MiB: bandwidth vs CTA count and bulk-ring depth (prints its own line)")
     ap.add_argument("--copy-engine", action="store_true",
                     help="AllGather by one device-to-device memcpy per (source, destination) pair, beside the kernel")
+    ap.add_argument("--policy-sweep", action="store_true",
+                    help="automatic chunk size against fixed chunk sizes, AllGather and AllReduce, T = 1 MiB .. 1 GiB")
     return ap.parse_args()
 
 
@@ -257,39 +259,42 @@ def time_sweep(ctx, wl, stream, torch):
         for name in ("allgather", "allreduce"):
             n = T // 2 // R if name == "allgather" else T // 2
             fn = getattr(wl, name)
-            for _ in range(3):
-                fn(ctx, stream.cuda_stream, n)
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            if T <= (64 << 20):
-                calls = 50 if T <= (4 << 20) else 10
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for _ in range(calls):
-                        fn(ctx, stream.cuda_stream, n)
-                with torch.cuda.stream(stream):
-                    g.replay()
-                    torch.cuda.synchronize()
-                    reps = 5
-                    a.record(stream)
-                    for _ in range(reps):
-                        g.replay()
-                    b.record(stream)
-                torch.cuda.synchronize()
-                us = a.elapsed_time(b) * 1e3 / (reps * calls)
-                how = "graph"
-            else:
-                reps = 5
-                a.record(stream)
-                for _ in range(reps):
-                    fn(ctx, stream.cuda_stream, n)
-                b.record(stream)
-                torch.cuda.synchronize()
-                us = a.elapsed_time(b) * 1e3 / reps
-                how = "events"
+            us, how = time_call(lambda: fn(ctx, stream.cuda_stream, n), T, stream, torch)
             row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
         out.append(row)
     return out
+
+
+def time_call(call, T, stream, torch):
+    """Mean device time of one `call` (which launches on `stream`) after 3
+    warm-ups: up to 64 MiB from a CUDA graph of 10-50 calls replayed 5 times
+    (no host launch overhead), above that from events around 5 calls."""
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    if T <= (64 << 20):
+        calls = 50 if T <= (4 << 20) else 10
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                call()
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * calls), "graph"
+    a.record(stream)
+    for _ in range(reps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps, "events"
 
 
 def run_e2e(ctx, wl, stream, torch, steps):
@@ -672,6 +677,60 @@ def run_depth_sweep(args):
     P.pl_ctx_destroy(ctx)
 
 
+def run_policy_sweep(args):
+    """The automatic chunk policy against fixed chunk sizes: AllGather and
+    AllReduce of the benchmark workload (R=8, bf16) at T = 1 MiB .. 1 GiB, each
+    with chunk_bytes = auto and 64 KiB .. 4 MiB (datapath automatic).  Prints,
+    per (collective, T), the time of every chunk size, the chunk the automatic
+    policy picked and its time relative to the best fixed size."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from copy_reduce_datapath_gb300 import purlin as P
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = Workload(GiB, dev)
+    ctx = P.pl_ctx_create(0, 0)
+    stream = torch.cuda.Stream()  # graph capture needs a stream other than the default one
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    chunks = [0, 64 << 10, 256 << 10, 1 << 20, 4 << 20]
+    rows = []
+    for e in (20, 23, 26, 28, 30):
+        T = 1 << e
+        for name in ("allgather", "allreduce"):
+            if name == "allgather":
+                n = T // 2 // R
+                lin, lout = wl._layouts(n)
+                ins, outs, op = wl.ag_in, wl.ag_out, "copy"
+                icount, ocount = [n] * R, [n * R] * R
+            else:
+                n = T // 2
+                lens = [n // R] * (R - 1) + [n - (n // R) * (R - 1)]
+                lin = lout = P.pl_layout_partitioned(R, lens)
+                ins, outs, op = wl.ar_in, wl.ar_out, "sum"
+                icount = ocount = [n] * R
+            row = {"collective": name, "T": T, "us": {}}
+            for cb in chunks:
+                pol = P.pl_policy_default(chunk_bytes=cb)
+
+                def call():
+                    P.pl_collective(ctx, lin, lout, op, "bf16", R, P.ptrs(ins), icount, P.ptrs(outs), ocount, pol,
+                                    stream.cuda_stream)
+                us, _ = time_call(call, T, stream, torch)
+                row["us"]["auto" if cb == 0 else str(cb)] = round(us, 2)
+            plan = P.pl_plan_create(lin, lout, op, "bf16", R, None, num_sms=sms)
+            row["auto_chunk_bytes"] = int(P.pl_plan_get_stats(plan).chunk_elems) * 2
+            P.pl_plan_destroy(plan)
+            fixed = {k: v for k, v in row["us"].items() if k != "auto"}
+            best = min(fixed, key=fixed.get)
+            row["best_fixed"] = int(best)
+            row["auto_over_best"] = round(row["us"]["auto"] / fixed[best], 3)
+            rows.append(row)
+    assert P.pl_ctx_status(ctx, stream.cuda_stream) == P.PL_OK
+    print(json.dumps({"sweep": "chunk_policy", "R": R, "dtype": "bf16", "rows": rows}), flush=True)
+    P.pl_ctx_destroy(ctx)
+
+
 def run_copy_engine(args):
     """AllGather (R=8, bf16, T bytes of output per rank) done by one contiguous
     device-to-device copy per (source, destination) pair -- the copy-engine
@@ -763,6 +822,8 @@ def main():
         run_depth_sweep(args)
     elif args.copy_engine:
         run_copy_engine(args)
+    elif args.policy_sweep:
+        run_policy_sweep(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":

@@ -561,30 +561,36 @@ __device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long
     fence_proxy_async();  // the async-proxy stores before the generic release that follows
 }
 
-// Every source of the segment sits the same q bytes (q != 0) past a 16-byte
-// boundary while the destinations are 16-byte aligned at `body`.  Each warp
-// step loads 32 consecutive aligned vectors of every source (one per lane),
-// adds them lane by lane (sum), and lanes 0..30 splice their result with the
-// next lane's into one destination vector: 31 outputs per 32 loaded vectors,
-// one load per source per vector and one realignment per output.  Aligned
-// vector nv is the last one that holds bytes of the row.
-template <int DT, bool MAXOP, bool SUM>
+// Every source of the segment sits the same q bytes past a 16-byte boundary
+// while the destinations are 16-byte aligned at `body`.  Each warp step loads
+// consecutive aligned vectors of every source (one per lane) and reduces them
+// lane by lane (sum or maximum); for q != 0 lanes 0..30 splice their result
+// with the next lane's into one destination vector (31 outputs per 32 loaded
+// vectors), for q == 0 all 32 lanes store their own.  One load per source per
+// vector and at most one realignment per output.  For q != 0 aligned vector
+// nv is the last one that holds bytes of the row; for q == 0, vector nv - 1.
+// The kernels for plans not proven aligned move every vector body through
+// here, aligned or not: one body instead of three keeps them within the
+// register budget.
+template <int DT, bool MAXOP, bool SUM, bool WIDE>
 __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                              size_t body, unsigned nv, int q, int tid, int nthr)
 {
-    constexpr int U = SUM ? 2 : 8;  // warp steps in flight per thread
-    constexpr int G = 4;            // sources in flight per step (sum)
+    constexpr int U = SUM ? (WIDE ? 1 : 2) : 8;  // warp steps in flight per thread
+    constexpr int G = SUM ? 8 / U : 1;           // sources in flight per step
     const int lane = tid & 31;
     const unsigned warp = (unsigned)tid >> 5;
-    const unsigned span = 31u * ((unsigned)nthr >> 5);
-    for (unsigned g0 = warp * 31u; g0 < nv; g0 += span * U) {
+    const unsigned per = q ? 31u : 32u;  // outputs per warp step
+    const unsigned span = per * ((unsigned)nthr >> 5);
+    const unsigned lim = q ? nv + 1u : nv;
+    for (unsigned g0 = warp * per; g0 < nv; g0 += span * U) {
         uint4 r[U];
         if constexpr (!SUM) {
             const char* base = SRC_ROW(sh, 0, row) + body - q;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const unsigned idx = g0 + u * span + lane;
-                r[u] = idx <= nv ? ld16(base + (size_t)idx * 16) : make_uint4(0, 0, 0, 0);
+                r[u] = idx < lim ? ld16(base + (size_t)idx * 16) : make_uint4(0, 0, 0, 0);
             }
         } else {
             Acc<DT, MAXOP> acc[U];
@@ -595,7 +601,7 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
                     const unsigned idx = g0 + u * span + lane;
 #pragma unroll
                     for (int g = 0; g < G; ++g)
-                        x[u][g] = (s0 + g < nsrc && idx <= nv)
+                        x[u][g] = (s0 + g < nsrc && idx < lim)
                                       ? ld16(SRC_ROW(sh, s0 + g, row) + body - q + (size_t)idx * 16)
                                       : make_uint4(0, 0, 0, 0);
                 }
@@ -618,14 +624,17 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            uint4 nb;
-            nb.x = __shfl_down_sync(0xffffffffu, r[u].x, 1);
-            nb.y = __shfl_down_sync(0xffffffffu, r[u].y, 1);
-            nb.z = __shfl_down_sync(0xffffffffu, r[u].z, 1);
-            nb.w = __shfl_down_sync(0xffffffffu, r[u].w, 1);
+            uint4 v = r[u];
+            if (q) {  // warp-uniform
+                uint4 nb;
+                nb.x = __shfl_down_sync(0xffffffffu, r[u].x, 1);
+                nb.y = __shfl_down_sync(0xffffffffu, r[u].y, 1);
+                nb.z = __shfl_down_sync(0xffffffffu, r[u].z, 1);
+                nb.w = __shfl_down_sync(0xffffffffu, r[u].w, 1);
+                v = realign(r[u], nb, q);
+            }
             const unsigned out = g0 + u * span + lane;
-            if (lane < 31 && out < nv) {
-                const uint4 v = realign(r[u], nb, q);
+            if ((unsigned)lane < per && out < nv) {
 #pragma unroll 1
                 for (unsigned long long m = mask; m; m &= m - 1) {
                     const int d = __ffsll((long long)m) - 1;
@@ -758,15 +767,16 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
             if (tid == 0)
                 bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
-        } else if (ALIGN || aligned)
+        } else if (ALIGN)
             copy_body<true, kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
         else
-            shifted_body<DT, false, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
+            shifted_body<DT, false, false, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
     } else if constexpr (REDUCE) {
-        if (ALIGN || aligned)
-            sum_body<DT, MAXOP, (OPS & kOpsWide) != 0>(sh, nsrc, mask, row, body, nv, tid, nthr);
+        constexpr bool WIDE = (OPS & kOpsWide) != 0;
+        if (ALIGN)
+            sum_body<DT, MAXOP, WIDE>(sh, nsrc, mask, row, body, nv, tid, nthr);
         else if (uniform)
-            shifted_body<DT, MAXOP, true>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
+            shifted_body<DT, MAXOP, true, WIDE>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
         else
             sum_mixed<DT, MAXOP>(sh, nsrc, mask, row, body, nv, tid, nthr);
     }

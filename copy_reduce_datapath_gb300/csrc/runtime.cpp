@@ -37,6 +37,13 @@ constexpr uint64_t kMaxChunkBytes = 4 << 20;
 constexpr uint64_t kTicketedChunkBytes = 256 << 10;
 constexpr uint64_t kBulkAutoBytes = 64ull << 20;  // automatic bulk-ring datapath from this many bytes moved
 constexpr int kItemsPerCta = 4;       // auto chunking aims at this many items per CTA
+constexpr int kGuidedDiv = 4;         // guided chunking: each item moves remaining / (kGuidedDiv x grid) bytes
+constexpr int kGuidedTailDiv = 16;    // ... down to a chunk of total / (kGuidedTailDiv x grid) bytes,
+constexpr uint64_t kGuidedTailMin = 64 << 10;   // kept within [kGuidedTailMin, kGuidedTailMax]
+constexpr uint64_t kGuidedTailMax = 256 << 10;
+constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA: one item per CTA
+constexpr uint64_t kChunkGrain = 256;           // automatic chunk sizes are multiples of this many bytes
+constexpr uint64_t kBulkChunkBytes = 256 << 10; // automatic chunks of plans the bulk ring will move
 constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threads x 128 registers)
 constexpr size_t kMaxCachedPlans = 1024;
 constexpr uint32_t kMaxUsesPerLaunch = (1u << 24) - 2;
@@ -503,6 +510,37 @@ std::vector<Chunk> make_chunks(const Transfer& t, uint64_t chunk_elems, uint64_t
     return out;
 }
 
+// Where the next chunk of a transfer starts.
+struct Cursor {
+    uint64_t row = 0, col = 0;
+};
+
+// The next chunk of about `target` elements of transfer t from `cu` (the
+// same cuts as make_chunks, with a size that may change from chunk to chunk).
+Chunk next_chunk(const Transfer& t, Cursor& cu, uint64_t target, uint64_t vec_elems)
+{
+    const Region& d0 = t.dsts[0];
+    const uint64_t cols = d0.cols;
+    if (d0.rows > 1 && cu.col == 0 && cols <= target) {
+        const uint64_t per = std::min<uint64_t>(std::max<uint64_t>(1, target / cols), d0.rows - cu.row);
+        Chunk c{cu.row, per, 0, cols};
+        cu.row += per;
+        return c;
+    }
+    const uint64_t dst_off = d0.offset + cu.row * d0.stride;
+    uint64_t n = target;
+    if (cu.col == 0)
+        n += (vec_elems - dst_off % vec_elems) % vec_elems;
+    n = std::min(n, cols - cu.col);
+    Chunk c{cu.row, 1, cu.col, n};
+    cu.col += n;
+    if (cu.col == cols) {
+        cu.col = 0;
+        ++cu.row;
+    }
+    return c;
+}
+
 class Builder {
 public:
     Builder(HostPlan& hp, int R) : hp_(hp), R_(R) {}
@@ -668,10 +706,114 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     }
 
     std::vector<std::vector<Chunk>> chunks(ts.size());
+    std::vector<std::pair<size_t, size_t>> order;  // (transfer, chunk) in creation order
     size_t max_chunks = 0;
-    for (size_t i = 0; i < ts.size(); ++i) {
-        chunks[i] = make_chunks(ts[i], chunk_elems, E);
-        max_chunks = std::max(max_chunks, chunks[i].size());
+    if (!ticketed && pol.chunk_bytes == 0) {
+        // Items that never wait on one another, automatic chunk size.  A CTA
+        // moves its items one after another and each item starts with a
+        // memory round trip that nothing overlaps, so:
+        //  - small messages (at most kOneItemBytes per CTA) get about one
+        //    item per CTA: each transfer is cut into its share of the grid;
+        //  - larger ones whose transfers all have one size and fan-out, and
+        //    those the bulk ring moves, are cut into equal chunks;
+        //  - the others are cut by guided self-scheduling: each next item
+        //    moves about remaining bytes / (kGuidedDiv x grid), so items
+        //    shrink toward the end of the list, and CTAs that claim them in
+        //    order as they finish (the claim rule below) end within one small
+        //    item of each other, whatever the partition lengths.  Transfers
+        //    take turns.
+        // Sizes are multiples of kChunkGrain bytes, so chunks after the first
+        // of a row start as aligned as the row's aligned start.
+        const uint64_t grain = std::max<uint64_t>(E, kChunkGrain / S);
+        auto round_grain = [&](uint64_t elems) { return std::max(grain, elems / grain * grain); };
+        std::vector<Cursor> cur(ts.size());
+        // One-row transfers of one size and fan-out cut into equal chunks are
+        // already balanced: about kItemsPerCta x grid items plus small row
+        // ends.  (Strided transfers balance better guided: measured.)
+        bool equal = true;
+        for (const Transfer& t : ts)
+            equal &= t.count == ts[0].count && t.srcs.size() == ts[0].srcs.size() &&
+                     t.dsts.size() == ts[0].dsts.size() && t.dsts[0].rows == 1;
+        // Copy-only one-row plans over 16-byte aligned regions that move
+        // enough bytes run on the bulk ring (see pl_collective), which streams
+        // best in chunks of kBulkChunkBytes (measured on GB300).
+        bool bulk = pol.datapath == PL_ATOM_BULK || pol.datapath_auto;
+        uint64_t moved = 0;
+        for (const Transfer& t : ts) {
+            bulk &= op == PL_COPY || t.srcs.size() == 1;
+            moved += t.count * S * (t.srcs.size() + t.dsts.size());
+            for (const auto* side : {&t.srcs, &t.dsts})
+                for (const Region& g : *side)
+                    bulk &= (g.offset * S) % 16 == 0 && g.rows == 1;
+        }
+        bulk &= pol.datapath == PL_ATOM_BULK || moved >= kBulkAutoBytes;
+        if (total_bytes / (uint64_t)full_grid <= kOneItemBytes) {
+            const uint64_t min_elems = round_grain(kMinChunkBytes / S);
+            for (size_t i = 0; i < ts.size(); ++i) {
+                if (ts[i].count == 0)
+                    continue;
+                const uint64_t share = std::max<uint64_t>(1, (uint64_t)full_grid * (ts[i].count * S) / total_bytes);
+                uint64_t target = (ts[i].count + share - 1) / share;
+                target = std::max(min_elems, (target + grain - 1) / grain * grain);
+                for (uint64_t left = ts[i].count; left > 0;) {
+                    const Chunk ch = next_chunk(ts[i], cur[i], target, E);
+                    chunks[i].push_back(ch);
+                    left -= ch.nrows * ch.ncols;
+                }
+            }
+            for (auto& cs : chunks)
+                max_chunks = std::max(max_chunks, cs.size());
+            for (size_t c = 0; c < max_chunks; ++c)
+                for (size_t ti = 0; ti < ts.size(); ++ti)
+                    if (c < chunks[ti].size())
+                        order.push_back({ti, c});
+        } else if (equal || bulk) {
+            const uint64_t elems = round_grain((bulk ? std::min(chunk_bytes, kBulkChunkBytes) : chunk_bytes) / S);
+            for (size_t i = 0; i < ts.size(); ++i) {
+                chunks[i] = make_chunks(ts[i], elems, E);
+                max_chunks = std::max(max_chunks, chunks[i].size());
+            }
+            for (size_t c = 0; c < max_chunks; ++c)
+                for (size_t ti = 0; ti < ts.size(); ++ti)
+                    if (c < chunks[ti].size())
+                        order.push_back({ti, c});
+        } else {
+            uint64_t rem_moved = 0;
+            std::vector<uint64_t> rem(ts.size()), w(ts.size());
+            for (size_t i = 0; i < ts.size(); ++i) {
+                rem[i] = ts[i].count;
+                w[i] = S * (ts[i].srcs.size() + ts[i].dsts.size());
+                rem_moved += rem[i] * w[i];
+            }
+            const uint64_t tail_bytes = std::min(std::max(total_bytes / ((uint64_t)full_grid * kGuidedTailDiv),
+                                                          kGuidedTailMin), kGuidedTailMax);
+            const uint64_t min_elems = round_grain(tail_bytes / S);
+            const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
+            for (size_t k = 0; rem_moved > 0; k = (k + 1) % ts.size()) {
+                if (rem[k] == 0)
+                    continue;
+                uint64_t target = rem_moved / ((uint64_t)full_grid * kGuidedDiv) / w[k];
+                target = std::min(std::max(round_grain(target), min_elems), max_elems);
+                const Chunk ch = next_chunk(ts[k], cur[k], target, E);
+                const uint64_t got = ch.nrows * ch.ncols;
+                chunks[k].push_back(ch);
+                order.push_back({k, chunks[k].size() - 1});
+                rem[k] -= got;
+                rem_moved -= got * w[k];
+            }
+            for (auto& cs : chunks)
+                max_chunks = std::max(max_chunks, cs.size());
+        }
+    } else {
+        for (size_t i = 0; i < ts.size(); ++i) {
+            chunks[i] = make_chunks(ts[i], chunk_elems, E);
+            max_chunks = std::max(max_chunks, chunks[i].size());
+        }
+        // row by row: chunk c of every transfer, then chunk c + 1
+        for (size_t c = 0; c < max_chunks; ++c)
+            for (size_t ti = 0; ti < ts.size(); ++ti)
+                if (c < chunks[ti].size())
+                    order.push_back({ti, c});
     }
 
     Builder b(hp, R);
@@ -718,10 +860,9 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         else
             rows[phase][row].push_back(Deferred{std::move(pend), kind, pop, ch});
     };
-    for (size_t c = 0; c < max_chunks; ++c) {
-        for (size_t ti = 0; ti < ts.size(); ++ti) {
-            if (c >= chunks[ti].size())
-                continue;
+    for (const auto& oc : order) {
+        {
+            const size_t ti = oc.first, c = oc.second;
             const Transfer& t = ts[ti];
             const Chunk& ch = chunks[ti][c];
             const uint64_t blk = ch.nrows * ch.ncols * S;
@@ -910,11 +1051,14 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         return PL_ERR_NOMEM;
 
     int ctas = pol.ctas ? pol.ctas : full_grid;
-    if (!tickets)
-        ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
-    else
-        ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
+    ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
     ctas = std::max(1, ctas);
+    // Claim rule: items are claimed in index order through the device ticket
+    // when they wait on one another, and also whenever there are more items
+    // than CTAs, so that a CTA that finishes early takes the next item
+    // (dynamic balance; the guided sizes above rely on it).  One item per CTA
+    // needs no ticket.
+    const bool claim_in_order = tickets || hp.items.size() > (size_t)ctas;
 
     pl_plan_stats& s = hp.stats;
     s.items = hp.items.size();
@@ -926,7 +1070,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     s.slot_elems = staged ? slot_elems : 0;
     s.ctas = ctas;
     s.threads = kThreads;
-    s.uses_tickets = tickets ? 1 : 0;
+    s.uses_tickets = claim_in_order ? 1 : 0;
     s.path = pol.path;
     s.bytes_read = bytes_read;
     s.bytes_written = bytes_written;
@@ -1155,7 +1299,8 @@ std::string plan_key(const pl_layout& in, const pl_layout& out, pl_op op, pl_dty
                      const ResolvedPolicy& rp)
 {
     uint64_t k[9] = {in.id, out.id, (uint64_t)op, (uint64_t)dt, (uint64_t)R, (uint64_t)rp.path,
-                     (uint64_t)rp.ar_form, ((uint64_t)rp.ctas << 32) | (uint64_t)(rp.datapath == PL_ATOM_BULK),
+                     (uint64_t)rp.ar_form,
+                     ((uint64_t)rp.ctas << 32) | ((uint64_t)rp.datapath_auto << 1) | (uint64_t)(rp.datapath == PL_ATOM_BULK),
                      rp.chunk_bytes};
     return std::string(reinterpret_cast<const char*>(k), sizeof k);
 }

@@ -149,7 +149,7 @@ def test_zero_staging_traffic_is_algorithmic():
     ar = plan_for(L, L, "sum", "bf16", R, P.pl_policy_default())
     st = P.pl_plan_get_stats(ar)
     assert (st.bytes_read, st.bytes_written) == (R * T, R * T)
-    assert st.uses_tickets == 0 and st.flags == 0
+    assert st.flags == 0
 
 
 def test_staged_plans_wait_only_on_earlier_items():
@@ -251,3 +251,51 @@ def test_one_byte_chunks_and_alignment():
     st = P.pl_plan_get_stats(pl)
     assert st.chunk_elems % 16 == 0
     assert st.bytes_read == sum(lens) and st.bytes_written == R * sum(lens)
+
+
+@pytest.mark.parametrize("scale", [1, 20])
+@pytest.mark.parametrize("kind", ["allgatherv", "reducescatterv", "alltoallv", "ulysses", "allreduce_max"])
+def test_automatic_chunking_covers_every_element(kind, scale):
+    """Automatic chunks of plans whose items never wait (zero-staging), on a
+    4-SM grid: about one item per CTA for small messages (scale 1: under
+    256 KiB per CTA), guided sizes that shrink along the list for larger ones
+    (scale 20), claimed in order once there are more items than CTAs.
+    Executed by the emulator, the result equals the oracle."""
+    R, dtype = 8, "bf16"
+    pol = P.pl_policy_default()
+    if kind == "allgatherv":
+        lens = synth.zipf_lengths(60001 * scale, R, 0.125, seed=40)
+        ins = [rand(dtype, 40, r, lens[r]) for r in range(R)]
+        lin, lout, op = P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy"
+        want = oracle.allgather(ins, dtype)
+    elif kind == "reducescatterv":
+        lens = synth.zipf_lengths(60001 * scale, R, 0.125, seed=41)
+        ins = [rand(dtype, 41, r, sum(lens)) for r in range(R)]
+        lin, lout, op = P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), "sum"
+        want = oracle.reducescatter(ins, lens, dtype)
+    elif kind == "alltoallv":
+        m = synth.zipf_matrix(7001 * scale, R, 0.125, seed=42)
+        ins = [rand(dtype, 42, r, sum(m[r])) for r in range(R)]
+        lin, lout, op = P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), "copy"
+        want = oracle.alltoall(ins, m, dtype)
+    elif kind == "ulysses":
+        S_, H, D = 40 * scale, 16, 24
+        ins = [rand(dtype, 43, r, S_ * H * D) for r in range(R)]
+        lin, lout, op = P.pl_layout_ulysses_in(R, S_, H, D), P.pl_layout_ulysses_out(R, S_, H, D), "copy"
+        want = oracle.ulysses_a2a(ins, S_, H, D, dtype)
+    else:
+        n = 50003 * scale
+        ins = [rand(dtype, 44, r, n) for r in range(R)]
+        L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
+        lin, lout, op = L, L, "max"
+        want = oracle.allreduce(ins, dtype, op="max")
+    pl = plan_for(lin, lout, op, dtype, R, pol)
+    st, items = plan_interp.load_plan(pl)
+    sizes = [it.rows * it.cols for it, _, _ in items]
+    assert st.uses_tickets == (1 if st.items > st.ctas else 0)
+    if scale > 1 and kind != "alltoallv":  # (64 short transfers on 4 SMs: one item each, in turn)
+        assert st.items > st.ctas
+        assert max(sizes) <= 2 * sizes[0]  # the list starts with its largest items
+        assert sum(sizes[: len(sizes) // 4]) >= sum(sizes[-(len(sizes) // 4):])  # and ends with small ones
+    outs = [np.zeros(len(w), NP[dtype]) for w in want]
+    run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=3)
