@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--case", default=None, choices=sorted(CASES),
                     help="time one collective of the other workloads instead of the step (prints its own line)")
     ap.add_argument("--policy", default="", help="policy overrides for --case, e.g. path=2,chunk_bytes=262144")
+    ap.add_argument("--scratch", type=int, default=1 << 30,
+                    help="scratch ring bytes of the context for --case with the staged path (path=2)")
     ap.add_argument("--depth-sweep", action="store_true",
                     help="Atom copy of 256 MiB: bandwidth vs CTA count and bulk-ring depth (prints its own line)")
     ap.add_argument("--copy-engine", action="store_true",
@@ -548,7 +550,7 @@ def run_case(args):
         k, v = kv.split("=")
         setattr(pol, k, int(v))
     Rr = 3 if args.case == "allreduce_r3_fp32" else R
-    ctx = P.pl_ctx_create(0, 1 << 30 if pol.path == P.PL_PATH_STAGED else 0)
+    ctx = P.pl_ctx_create(0, args.scratch if pol.path == P.PL_PATH_STAGED else 0)
     T = args.T
     N = T // S
 
@@ -626,6 +628,7 @@ def run_case(args):
     us = a.elapsed_time(b) * 1e3 / max(1, args.steps)
     peak, kind_peak = measured_peaks()
     print(json.dumps({"case": args.case, "workload": desc, "T_bytes": T, "policy": args.policy or "default",
+                      "scratch_bytes": args.scratch if pol.path == P.PL_PATH_STAGED else 0,
                       "steps": args.steps, "us": round(us, 2), "algbw_GBps": round(T / us / 1e3, 2),
                       "hbm_GBps": round(moved / us / 1e3, 1), "frac_of_peak": round(moved / us / 1e3 / peak, 4),
                       "peak_GBps": peak, "peak_kind": kind_peak}), flush=True)
