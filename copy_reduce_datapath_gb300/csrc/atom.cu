@@ -34,13 +34,15 @@ cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages,
     }
 }
 
-int snac_ctas_per_sm(bool bulk, int stages)
+int snac_ctas_per_sm(bool aligned)
 {
-    (void)bulk;
-    (void)stages;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, false>,
-                                                      kThreads, 0) != cudaSuccess) {
+    const cudaError_t e =
+        aligned ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, true>,
+                                                                kThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, false>,
+                                                                kThreadsSpliced, 0);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

@@ -44,7 +44,11 @@ constexpr uint64_t kGuidedTailMax = 256 << 10;
 constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA: one item per CTA
 constexpr uint64_t kChunkGrain = 256;           // automatic chunk sizes are multiples of this many bytes
 constexpr uint64_t kBulkChunkBytes = 256 << 10; // automatic chunks of plans the bulk ring will move
-constexpr int kDefaultCtasPerSm = 1;  // occupancy of the SNAC kernel (512 threads x 128 registers)
+// CTAs per SM of the SNAC kernels for aligned plans and for other plans.
+struct Occupancy {
+    int aligned = kCtasPerSmAligned;
+    int spliced = kCtasPerSmSpliced;
+};
 constexpr size_t kMaxCachedPlans = 1024;
 constexpr uint32_t kMaxUsesPerLaunch = (1u << 24) - 2;
 
@@ -647,7 +651,7 @@ bool waits_precede(const HostPlan& hp)
 // Derives the work list with consumers emitted `lag` chunk rows behind the
 // producers they wait for (so the CTAs that claim them in order rarely spin).
 pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
-                       const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, int lag,
+                       const ResolvedPolicy& pol, int num_sms, Occupancy occ, uint64_t scratch_bytes, int lag,
                        HostPlan& hp)
 {
     if (in.R != R || out.R != R)
@@ -669,7 +673,14 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         total_bytes += t.count * S;
     }
 
-    const int full_grid = std::max(1, num_sms) * std::max(1, ctas_per_sm);
+    // Plans whose regions are all 16-byte aligned run the aligned kernels, the
+    // others the spliced ones, each with its own CTAs per SM.
+    bool regions_aligned = true;
+    for (const Transfer& t : ts)
+        for (const auto* side : {&t.srcs, &t.dsts})
+            for (const Region& g : *side)
+                regions_aligned &= (g.offset * S) % 16 == 0 && (g.rows == 1 || (g.stride * S) % 16 == 0);
+    const int full_grid = std::max(1, num_sms) * std::max(1, regions_aligned ? occ.aligned : occ.spliced);
     uint64_t chunk_bytes = pol.chunk_bytes;
     if (chunk_bytes == 0) {
         chunk_bytes = total_bytes / ((uint64_t)full_grid * kItemsPerCta);
@@ -678,14 +689,16 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     chunk_bytes = std::max<uint64_t>(256, chunk_bytes / 256 * 256);
 
     const bool staged = pol.path == PL_PATH_STAGED;
-    // Plans whose items wait on one another keep about one grid of chunks in
-    // flight between a producer and its consumers; small chunks keep those
-    // bytes resident in L2, so consumers read them from there.
     bool multi_dst_sum = false;
     for (const Transfer& t : ts)
         multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
     const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
-    if (ticketed && pol.chunk_bytes == 0)
+    // The staged path keeps chunks small, so that a ring of a given size holds
+    // many rows of them (measured: the staged AllReduce does not gain from
+    // larger chunks, the staged ReduceScatter loses).  The zero-staging
+    // composed form takes the general rule (it gains from large chunks: at
+    // 1 GiB, 256 KiB chunks ran at 0.68 of the roofline, 4 MiB at 0.79).
+    if (staged && pol.chunk_bytes == 0)
         chunk_bytes = std::min<uint64_t>(chunk_bytes, kTicketedChunkBytes);
     if (staged && pol.chunk_bytes == 0) {
         uint64_t per_rank = scratch_bytes / (uint64_t)R;
@@ -1081,13 +1094,13 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
 // ring cannot hold (a slot would be reused before its consumers) or that
 // breaks the claim-order rule falls back to smaller ones, down to none.
 pl_status derive(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
-                 const ResolvedPolicy& pol, int num_sms, int ctas_per_sm, uint64_t scratch_bytes, HostPlan& hp)
+                 const ResolvedPolicy& pol, int num_sms, Occupancy occ, uint64_t scratch_bytes, HostPlan& hp)
 {
-    pl_status st = derive_order(in, out, op, dt, R, pol, num_sms, ctas_per_sm, scratch_bytes, -1, hp);
+    pl_status st = derive_order(in, out, op, dt, R, pol, num_sms, occ, scratch_bytes, -1, hp);
     if (st != PL_ERR_NOMEM)
         return st;
     for (int lag = hp.lag / 2; lag >= 0; lag = lag > 1 ? lag / 2 : lag - 1) {
-        st = derive_order(in, out, op, dt, R, pol, num_sms, ctas_per_sm, scratch_bytes, lag, hp);
+        st = derive_order(in, out, op, dt, R, pol, num_sms, occ, scratch_bytes, lag, hp);
         if (st != PL_ERR_NOMEM)
             return st;
     }
@@ -1120,7 +1133,7 @@ PL_API pl_status pl_plan_create(pl_plan** plan, const pl_layout* in, const pl_la
     std::unique_ptr<pl_plan> p(new (std::nothrow) pl_plan);
     if (!p)
         return PL_ERR_NOMEM;
-    st = derive(*in, *out, op, dtype, R, rp, num_sms, kDefaultCtasPerSm, scratch_bytes, p->hp);
+    st = derive(*in, *out, op, dtype, R, rp, num_sms, Occupancy{}, scratch_bytes, p->hp);
     if (st != PL_OK)
         return st;
     *plan = p.release();
@@ -1233,7 +1246,7 @@ private:
 struct pl_ctx {
     int device = 0;
     int num_sms = 0;
-    int ctas_per_sm = kDefaultCtasPerSm;
+    Occupancy occ;
     void* state_mem = nullptr;
     DeviceState st{};
     uint32_t flag_capacity = 0;
@@ -1317,7 +1330,7 @@ pl_status get_plan(pl_ctx* ctx, const pl_layout& in, const pl_layout& out, pl_op
     std::unique_ptr<DevicePlan> p(new (std::nothrow) DevicePlan);
     if (!p)
         return PL_ERR_NOMEM;
-    pl_status st = derive(in, out, op, dt, R, rp, ctx->num_sms, ctx->ctas_per_sm, ctx->scratch_bytes, p->hp);
+    pl_status st = derive(in, out, op, dt, R, rp, ctx->num_sms, ctx->occ, ctx->scratch_bytes, p->hp);
     if (st != PL_OK)
         return st;
     size_t bi = p->hp.items.size() * sizeof(Item);
@@ -1445,9 +1458,11 @@ PL_API pl_status pl_ctx_create(pl_ctx** out, int device, uint64_t scratch_bytes)
     cudaError_t e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess)
         return cuda_fail(ctx.get(), e);
-    int occ = snac_ctas_per_sm(false, 0);
-    if (occ > 0)
-        ctx->ctas_per_sm = std::min(occ, kDefaultCtasPerSm);
+    const int occ_aligned = snac_ctas_per_sm(true), occ_spliced = snac_ctas_per_sm(false);
+    if (occ_aligned > 0)
+        ctx->occ.aligned = std::min(occ_aligned, kCtasPerSmAligned);
+    if (occ_spliced > 0)
+        ctx->occ.spliced = std::min(occ_spliced, kCtasPerSmSpliced);
     pl_status st = ensure_flags(ctx.get(), 4096);
     if (st != PL_OK)
         return st;
@@ -1569,7 +1584,10 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         if (rp.stages_auto)
             stages = kBulkMaxStages;
     }
-    cudaError_t e = launch_snac(a, ps.ctas, bulk, stages, (cudaStream_t)stream);
+    // The bulk ring's shared memory holds one CTA per SM: a grid sized for the
+    // two-CTA spliced kernels is trimmed to one CTA per SM (claims adapt).
+    const int ctas = bulk && !dp->hp.all_aligned ? std::min(ps.ctas, ctx->num_sms) : ps.ctas;
+    cudaError_t e = launch_snac(a, ctas, bulk, stages, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(ctx, e);
     ++ctx->launches;
@@ -1633,7 +1651,7 @@ int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bu
     if ((st = resolve_policy(&pol, rp)) != PL_OK)
         return st;
     HostPlan hp;
-    if ((st = derive(*L, *L, PL_SUM, (pl_dtype)dtype, R, rp, num_sms, kDefaultCtasPerSm, ring_bytes, hp)) != PL_OK)
+    if ((st = derive(*L, *L, PL_SUM, (pl_dtype)dtype, R, rp, num_sms, Occupancy{}, ring_bytes, hp)) != PL_OK)
         return st;
     out.items = std::move(hp.items);
     out.refs = std::move(hp.refs);

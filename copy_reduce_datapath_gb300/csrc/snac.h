@@ -12,8 +12,17 @@ namespace purlin {
 
 constexpr int kMaxRanks = 64;
 constexpr int kMaxRefsPerItem = 2 * kMaxRanks + 1;  // R sources + R destinations + one slot
-constexpr int kThreads = 512;                        // threads per CTA of the persistent grid
+constexpr int kThreads = 512;                        // threads per CTA of the kernels for aligned plans
+constexpr int kThreadsSpliced = 512;                 // threads per CTA of the kernels for other plans
+static_assert(kThreads >= kMaxRefsPerItem && kThreadsSpliced >= kMaxRefsPerItem,
+              "one thread per region reference of an item");
 constexpr int kBulkMaxStages = 8;
+// CTAs per SM the kernels are built for: those for plans proven 16-byte
+// aligned keep 128 registers per thread; those for other plans (every body
+// through the warp-spliced path) run two CTAs per SM at 64 registers, whose
+// extra warps hide the splice and reduce arithmetic between memory waits.
+constexpr int kCtasPerSmAligned = 1;
+constexpr int kCtasPerSmSpliced = 2;
 
 enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2 };
 enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3 };
@@ -110,8 +119,8 @@ cudaError_t launch_snac_fp16(const LaunchArgs& a, int ctas, bool bulk, bool alig
 cudaError_t launch_snac_fp32(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
 cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
 
-// CTAs of the SNAC kernel that fit on one SM at once.
-int snac_ctas_per_sm(bool bulk, int stages);
+// CTAs of the SNAC kernel for aligned (or other) plans that fit on one SM at once.
+int snac_ctas_per_sm(bool aligned);
 
 // Host-side work list of a staged AllReduce whose device state lives in
 // caller-provided memory (runtime.cpp; used by the allocation-free entry point).

@@ -284,7 +284,7 @@ def test_automatic_chunking_covers_every_element(kind, scale):
         lin, lout, op = P.pl_layout_ulysses_in(R, S_, H, D), P.pl_layout_ulysses_out(R, S_, H, D), "copy"
         want = oracle.ulysses_a2a(ins, S_, H, D, dtype)
     else:
-        n = 50003 * scale
+        n = 100003 * scale
         ins = [rand(dtype, 44, r, n) for r in range(R)]
         L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
         lin, lout, op = L, L, "max"
