@@ -212,6 +212,21 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// At most n bulk groups of this thread still reading their shared memory (n < 8).
+__device__ __forceinline__ void bulk_wait_read_n(int n)
+{
+    switch (n) {
+    case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    }
+}
+
+__device__ __forceinline__ uint4 lds16(const char* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void sts16(char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // Bounded wait for the phase `parity` of an mbarrier.
 __device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const LaunchArgs& a)
@@ -228,14 +243,29 @@ __device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const Launch
 }
 
 // The CTA's bulk-copy ring: `stages` buffers of kBulkPiece bytes, one mbarrier
-// each.  Only thread 0 touches it; `phase` holds the parity each stage's
-// barrier will complete next.
+// each.  bulk_copy (thread 0 alone) tracks in `phase` the parity each stage's
+// barrier will complete next.  bulk_shift_copy (every thread) uses the same
+// buffers in pairs and its own barriers `sbar` with parities `sphase`, which
+// every thread keeps identically.
 struct BulkRing {
     char* buf;
     unsigned long long* bar;
     int stages;
     unsigned phase;
+    unsigned long long* sbar;
+    unsigned sphase;
 };
+
+// End of a bulk move: every store has landed, and the async-proxy stores are
+// ordered before the generic release that may follow.  (Waiting only until
+// the stores had read the ring, so that they overlap the next item's loads,
+// measured no faster.)
+__device__ __forceinline__ void bulk_finish()
+{
+    bulk_wait_all();
+    fence_proxy_async();
+}
+constexpr int kShiftMaxDepth = kBulkMaxStages / 2;
 
 // ------------------------------------------------------------- element math
 
@@ -556,8 +586,88 @@ __device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long
                 bk.phase ^= 1u << sidx;
         }
     }
-    bulk_wait_all();
-    fence_proxy_async();  // the async-proxy stores before the generic release that follows
+    bulk_finish();
+}
+
+// Copy of nv output vectors from one source that sits q bytes (q != 0) past
+// a 16-byte boundary to every destination in `mask` (16-byte aligned at
+// `body`), through the shared-memory ring, by the whole CTA.  The ring's
+// buffers pair up (depth = stages / 2 >= 2 pairs): piece p of 1023 output
+// vectors is loaded (aligned source vectors p * 1023 .. p * 1023 + 1023, one
+// more than it outputs) into the first buffer of pair p % depth by one bulk
+// copy, realigned by every thread into the second buffer, and stored from
+// there to each destination by one bulk copy.  Thread 0 keeps up to `depth`
+// loads in flight; before the barrier of piece p it waits until the stores
+// that last read the output buffer of piece p + 1 are done.  Every thread
+// waits on the same barriers and takes the same branches (the barrier of each
+// piece ANDs the waits' outcomes), so a load that never completes ends the
+// copy for every thread at the same piece; thread 0 then waits, bounded, for
+// the loads still in flight (the status word reports the timeout).
+__device__ void bulk_shift_copy(BulkRing& bk, const ItemShared& sh, unsigned long long mask, unsigned row,
+                                size_t body, const char* src_al, int q, unsigned nv, int tid, int nthr,
+                                const LaunchArgs& a)
+{
+    constexpr unsigned kOut = kBulkPiece / 16 - 1;  // output vectors per piece
+    const unsigned depth = (unsigned)bk.stages / 2;
+    const unsigned np = (nv + kOut - 1) / kOut;
+    auto inb = [&](unsigned i) { return bk.buf + (size_t)(2 * i) * kBulkPiece; };
+    auto outb = [&](unsigned i) { return bk.buf + (size_t)(2 * i + 1) * kBulkPiece; };
+    auto nout_of = [&](unsigned p) { return min(kOut, nv - p * kOut); };
+    auto load = [&](unsigned p) {
+        const unsigned i = p % depth;
+        const unsigned bytes = (nout_of(p) + 1u) * 16u;  // the last aligned vector still holds bytes of the row
+        mbar_expect_tx(&bk.sbar[i], bytes);
+        bulk_g2s(inb(i), src_al + (size_t)p * kOut * 16, bytes, &bk.sbar[i]);
+    };
+    unsigned issued = 0, waited = 0;  // thread 0's count of loads issued and of barrier waits passed
+    if (tid == 0) {
+        fence_proxy_async();  // earlier generic writes (after a flag acquire) before the async loads
+        for (; issued < np && issued < depth; ++issued)
+            load(issued);
+    }
+    bool all_ok = true;
+    for (unsigned p = 0; p < np; ++p) {
+        const unsigned i = p % depth;
+        const bool ok = mbar_wait(&bk.sbar[i], (bk.sphase >> i) & 1u, a);
+        if (ok) {
+            bk.sphase ^= 1u << i;
+            ++waited;
+            const char* in = inb(i);
+            char* out = outb(i);
+            const unsigned nout = nout_of(p);
+            for (unsigned v = (unsigned)tid; v < nout; v += (unsigned)nthr)
+                sts16(out + (size_t)v * 16, realign(lds16(in + (size_t)v * 16), lds16(in + (size_t)v * 16 + 16), q));
+        }
+        fence_proxy_async_smem();  // the realigned vectors before the bulk stores that read them
+        if (tid == 0)
+            bulk_wait_read_n((int)depth - 2);
+        all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        if (!all_ok)
+            break;
+        if (tid == 0) {
+            const unsigned nout = nout_of(p);
+#pragma unroll 1
+            for (unsigned long long m = mask; m; m &= m - 1) {
+                const int d = __ffsll((long long)m) - 1;
+                bulk_s2g(DST_ROW(sh, d, row) + body + (size_t)p * kOut * 16, outb(i), nout * 16u);
+            }
+            bulk_commit();
+            if (issued < np) {
+                fence_proxy_async_smem();  // every thread read this input buffer before the barrier
+                load(issued);
+                ++issued;
+            }
+        }
+    }
+    if (tid == 0) {
+        // After a timeout, the loads still in flight land before the ring is reused.
+        for (; !all_ok && waited < issued; ++waited) {
+            const unsigned i = waited % depth;
+            if (mbar_wait(&bk.sbar[i], (bk.sphase >> i) & 1u, a))
+                bk.sphase ^= 1u << i;
+        }
+        bulk_finish();
+    }
 }
 
 // Every source of the segment sits the same q bytes past a 16-byte boundary
@@ -766,10 +876,14 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
             if (tid == 0)
                 bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
-        } else if (ALIGN)
+        } else if constexpr (ALIGN) {
             copy_body<true, kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
-        else
+        } else if (BULK && nthr == (int)blockDim.x && bk.stages >= 4 && nv * 16u >= kBulkMin) {
+            // a source misaligned against aligned destinations (q0 != 0 here)
+            bulk_shift_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body - q0, q0, nv, tid, nthr, a);
+        } else {
             shifted_body<DT, false, false, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
+        }
     } else if constexpr (REDUCE) {
         constexpr bool WIDE = (OPS & kOpsWide) != 0;
         if (ALIGN)
@@ -1010,12 +1124,15 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     __shared__ __align__(16) Ref sref[ALIGN ? kMaxRefsPerItem : 1];
     __shared__ int s_ok;
     extern __shared__ __align__(128) char dyn[];
-    BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u};
+    BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u,
+                reinterpret_cast<unsigned long long*>(dyn) + kBulkMaxStages, 0u};
     const int tid = (int)threadIdx.x;
     if (tid == 0) {
         if (BULK) {
             for (int i = 0; i < stages; ++i)
                 mbar_init(&bk.bar[i], 1u);
+            for (int i = 0; i < kShiftMaxDepth; ++i)
+                mbar_init(&bk.sbar[i], 1u);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
         const unsigned i0 = claim(a, 0);

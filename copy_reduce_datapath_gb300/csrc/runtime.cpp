@@ -781,9 +781,26 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                     if (c < chunks[ti].size())
                         order.push_back({ti, c});
         } else if (equal || bulk) {
-            const uint64_t elems = round_grain((bulk ? std::min(chunk_bytes, kBulkChunkBytes) : chunk_bytes) / S);
+            // k items per CTA (kItemsPerCta, or enough to keep chunks within
+            // the cap), each transfer cut into floor(its share of k x grid)
+            // near-equal chunks: at most k items per CTA, none much larger
+            // than total / (k x grid).
+            const uint64_t cap = bulk ? kBulkChunkBytes : kMaxChunkBytes;
+            const uint64_t per_cta = (total_bytes + (uint64_t)full_grid - 1) / (uint64_t)full_grid;
+            const uint64_t k = std::max<uint64_t>((per_cta + cap - 1) / cap, kItemsPerCta);
+            const uint64_t items = k * (uint64_t)full_grid;
             for (size_t i = 0; i < ts.size(); ++i) {
-                chunks[i] = make_chunks(ts[i], elems, E);
+                if (ts[i].count == 0)
+                    continue;
+                const uint64_t share = std::max<uint64_t>(1, (uint64_t)((double)items * (double)(ts[i].count * S) /
+                                                                        (double)total_bytes));
+                uint64_t target = (ts[i].count + share - 1) / share;
+                target = (target + grain - 1) / grain * grain;
+                for (uint64_t left = ts[i].count; left > 0;) {
+                    const Chunk ch = next_chunk(ts[i], cur[i], target, E);
+                    chunks[i].push_back(ch);
+                    left -= ch.nrows * ch.ncols;
+                }
                 max_chunks = std::max(max_chunks, chunks[i].size());
             }
             for (size_t c = 0; c < max_chunks; ++c)
@@ -1572,13 +1589,17 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         a.bufs[R + r] = (char*)out_bufs[r];
     }
     a.bufs[2 * R] = ctx->scratch;
-    // Codesign policy for the datapath: large copy-only plans over 16-byte
-    // aligned regions stream through the bulk-copy ring (one shared-memory
-    // read per chunk, one bulk store per destination); everything else uses
-    // the vector datapath.
+    // Codesign policy for the datapath: large copy-only plans stream through
+    // the bulk-copy ring (one shared-memory read per chunk, one bulk store per
+    // destination) when their regions are 16-byte aligned, or when they write
+    // at least twice what they read (a broadcast, the AllGather(V) shape:
+    // misaligned sources are then realigned in shared memory between the
+    // bulk load and the bulk stores); everything else uses the vector
+    // datapath.
     bool bulk = rp.datapath == PL_ATOM_BULK;
     int stages = rp.stages;
-    if (rp.datapath_auto && dp->hp.ops == kOpsCopy && dp->hp.all_aligned &&
+    if (rp.datapath_auto && dp->hp.ops == kOpsCopy &&
+        (dp->hp.all_aligned || ps.bytes_written >= 2 * ps.bytes_read) &&
         ps.bytes_read + ps.bytes_written >= kBulkAutoBytes) {
         bulk = true;
         if (rp.stages_auto)

@@ -109,10 +109,13 @@ typedef struct pl_policy {
 #define PL_AR_FUSED     1 /* one work item reduces a chunk and writes it to every output of its name */
 #define PL_AR_COMPOSED  2 /* Figure 6: the owner reduces its partition's chunk, notifies, the others gather it */
 
-#define PL_ATOM_AUTO    0 /* bulk ring (8 stages) for copy-only plans over 16-byte aligned regions moving >= 64 MiB,
-                             vector otherwise */
+#define PL_ATOM_AUTO    0 /* bulk ring (8 stages) for copy-only plans moving >= 64 MiB whose regions are 16-byte
+                             aligned or that write at least twice what they read; vector otherwise */
 #define PL_ATOM_VECTOR  1 /* 16-byte vector loads and stores by every thread */
-#define PL_ATOM_BULK    2 /* cp.async.bulk through a shared-memory ring (COPY work items; others use vector) */
+#define PL_ATOM_BULK    2 /* cp.async.bulk through a shared-memory ring for COPY work items: aligned sources
+                             directly; sources at a byte shift from their destinations realigned in shared
+                             memory between the bulk load and the bulk stores (4 stages or more); other
+                             items use the vector datapath */
 
 /* Fills *pol with the all-auto policy (debug_drop_notify = -1). */
 PL_API void pl_policy_default(pl_policy* pol);

@@ -347,6 +347,26 @@ def test_bulk_ring_datapath(ctx, stages):
         assert_equal(got[j], want[j], f"Ulysses rank {j}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("stages", [0, 4, 6, 8])
+def test_bulk_shift_copy(ctx, dtype, stages):
+    """Copies whose source sits at a byte shift from the (aligned) destinations
+    through the bulk ring: bulk load, realignment in shared memory, bulk stores.
+    AllGatherV with Zipf lengths (every shift, odd ones for one-byte elements),
+    ragged last pieces; stages = 0 is the automatic policy (chosen for
+    write-heavy copies of 64 MiB or more)."""
+    R = 8
+    pol = P.pl_policy_default(datapath=P.PL_ATOM_AUTO if stages == 0 else P.PL_ATOM_BULK, stages=stages)
+    N = (8 << 20) // (1 if dtype == "fp8" else 2) + 13  # 8 MiB per output: 72 MiB moved
+    lens = synth.zipf_lengths(N, R, 0.125, seed=50 + stages)
+    ins = [host(None if dtype == "fp8" else "normal", dtype, 50, r, lens[r]) for r in range(R)]
+    got = run(ctx, P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy", dtype, ins,
+              [N] * R, pol)
+    want = oracle.allgather(ins, dtype)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"AGV rank {r}")
+
+
 @pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
 def test_bulk_ring_in_flagged_paths(ctx, form):
     """Bulk copies inside staged and composed plans (stage, gather) with flags."""
