@@ -43,7 +43,9 @@ constexpr uint64_t kGuidedTailMin = 64 << 10;   // kept within [kGuidedTailMin, 
 constexpr uint64_t kGuidedTailMax = 256 << 10;
 constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA: one item per CTA
 constexpr uint64_t kChunkGrain = 256;           // automatic chunk sizes are multiples of this many bytes
-constexpr uint64_t kBulkChunkBytes = 256 << 10; // automatic chunks of plans the bulk ring will move
+constexpr uint64_t kBulkItemBytes = 512 << 10;  // bytes (read + written) of an automatic bulk-ring item
+constexpr uint64_t kBulkChunkMin = 64 << 10;    // ... whose chunk stays within these
+constexpr uint64_t kBulkChunkMax = 256 << 10;
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
@@ -673,6 +675,30 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         total_bytes += t.count * S;
     }
 
+    // One-row copy plans the bulk ring will move (the rule of
+    // pl_collective: forced, or automatic for plans moving at least
+    // kBulkAutoBytes whose regions are 16-byte aligned or that write at
+    // least twice what they read) stream best in items that move about
+    // kBulkItemBytes (measured on GB300: an AllGather at 1 GiB, one source
+    // and eight destinations, best with 64 KiB chunks; the MoE AllToAll,
+    // one and one, with 256 KiB).
+    bool bulk = pol.datapath == PL_ATOM_BULK || pol.datapath_auto;
+    bool all_aligned_regions = true;
+    uint64_t moved = 0, rd = 0, wr = 0, fanout = 2;
+    for (const Transfer& t : ts) {
+        bulk &= op == PL_COPY || t.srcs.size() == 1;
+        moved += t.count * S * (t.srcs.size() + t.dsts.size());
+        rd += t.count * S * t.srcs.size();
+        wr += t.count * S * t.dsts.size();
+        fanout = std::max<uint64_t>(fanout, t.srcs.size() + t.dsts.size());
+        for (const auto* side : {&t.srcs, &t.dsts})
+            for (const Region& g : *side) {
+                bulk &= g.rows == 1;
+                all_aligned_regions &= (g.offset * S) % 16 == 0;
+            }
+    }
+    bulk &= pol.datapath == PL_ATOM_BULK ||
+            (moved >= kBulkAutoBytes && (all_aligned_regions || wr >= 2 * rd));
     // Plans whose regions are all 16-byte aligned run the aligned kernels, the
     // others the spliced ones, each with its own CTAs per SM.
     bool regions_aligned = true;
@@ -680,7 +706,8 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         for (const auto* side : {&t.srcs, &t.dsts})
             for (const Region& g : *side)
                 regions_aligned &= (g.offset * S) % 16 == 0 && (g.rows == 1 || (g.stride * S) % 16 == 0);
-    const int full_grid = std::max(1, num_sms) * std::max(1, regions_aligned ? occ.aligned : occ.spliced);
+    // (The bulk ring's shared memory holds one CTA per SM, whatever the kernel.)
+    const int full_grid = std::max(1, num_sms) * std::max(1, regions_aligned || bulk ? occ.aligned : occ.spliced);
     uint64_t chunk_bytes = pol.chunk_bytes;
     if (chunk_bytes == 0) {
         chunk_bytes = total_bytes / ((uint64_t)full_grid * kItemsPerCta);
@@ -716,6 +743,15 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         slots_per_rank = per_rank / (slot_elems * S);
         if (slots_per_rank < 2)
             return PL_ERR_NOMEM;
+        // A whole number of rows of one rank's stages, so that the stages a
+        // rank makes in one row never wrap around its ring (they merge, below).
+        std::vector<uint64_t> per_row(R, 0);
+        for (const Transfer& t : ts)
+            for (const Region& g : t.srcs)
+                ++per_row[g.rank];
+        const uint64_t g = *std::max_element(per_row.begin(), per_row.end());
+        if (g > 1 && slots_per_rank >= 2 * g)
+            slots_per_rank = slots_per_rank / g * g;
     }
 
     std::vector<std::vector<Chunk>> chunks(ts.size());
@@ -728,7 +764,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         //  - small messages (at most kOneItemBytes per CTA) get about one
         //    item per CTA: each transfer is cut into its share of the grid;
         //  - larger ones whose transfers all have one size and fan-out, and
-        //    those the bulk ring moves, are cut into equal chunks;
+        //    aligned ones the bulk ring moves, are cut into equal chunks;
         //  - the others are cut by guided self-scheduling: each next item
         //    moves about remaining bytes / (kGuidedDiv x grid), so items
         //    shrink toward the end of the list, and CTAs that claim them in
@@ -747,19 +783,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         for (const Transfer& t : ts)
             equal &= t.count == ts[0].count && t.srcs.size() == ts[0].srcs.size() &&
                      t.dsts.size() == ts[0].dsts.size() && t.dsts[0].rows == 1;
-        // Copy-only one-row plans over 16-byte aligned regions that move
-        // enough bytes run on the bulk ring (see pl_collective), which streams
-        // best in chunks of kBulkChunkBytes (measured on GB300).
-        bool bulk = pol.datapath == PL_ATOM_BULK || pol.datapath_auto;
-        uint64_t moved = 0;
-        for (const Transfer& t : ts) {
-            bulk &= op == PL_COPY || t.srcs.size() == 1;
-            moved += t.count * S * (t.srcs.size() + t.dsts.size());
-            for (const auto* side : {&t.srcs, &t.dsts})
-                for (const Region& g : *side)
-                    bulk &= (g.offset * S) % 16 == 0 && g.rows == 1;
-        }
-        bulk &= pol.datapath == PL_ATOM_BULK || moved >= kBulkAutoBytes;
+        const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / fanout, kBulkChunkMin), kBulkChunkMax);
         if (total_bytes / (uint64_t)full_grid <= kOneItemBytes) {
             const uint64_t min_elems = round_grain(kMinChunkBytes / S);
             for (size_t i = 0; i < ts.size(); ++i) {
@@ -780,12 +804,12 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                 for (size_t ti = 0; ti < ts.size(); ++ti)
                     if (c < chunks[ti].size())
                         order.push_back({ti, c});
-        } else if (equal || bulk) {
+        } else if (equal || (bulk && all_aligned_regions)) {
             // k items per CTA (kItemsPerCta, or enough to keep chunks within
             // the cap), each transfer cut into floor(its share of k x grid)
             // near-equal chunks: at most k items per CTA, none much larger
             // than total / (k x grid).
-            const uint64_t cap = bulk ? kBulkChunkBytes : kMaxChunkBytes;
+            const uint64_t cap = bulk && all_aligned_regions ? bulk_chunk : kMaxChunkBytes;
             const uint64_t per_cta = (total_bytes + (uint64_t)full_grid - 1) / (uint64_t)full_grid;
             const uint64_t k = std::max<uint64_t>((per_cta + cap - 1) / cap, kItemsPerCta);
             const uint64_t items = k * (uint64_t)full_grid;
@@ -1025,10 +1049,74 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         }
     }
 
+    // Staged fused AllReduce (every transfer has as many destinations as
+    // sources): the stages one source rank makes in one chunk row (its chunk
+    // of each partition, equally spaced in its buffer, into consecutive slots
+    // of its ring) become one multi-row item, which moves as many bytes as a
+    // consume item: at R = 8 a row of 64 stage items and 8 consume items
+    // becomes 8 and 8 (measured 7% faster).  Where consume items are lighter
+    // (ReduceScatter: 8 sources, 1 destination) or re-stage (the composed
+    // form), merged stages measured 8-11% slower, so they stay one per chunk.
+    bool merge_stages = staged && lag != 0 && pol.ar_form != PL_AR_COMPOSED;
+    for (const Transfer& t : ts)
+        merge_stages &= t.dsts.size() == t.srcs.size();
+    if (merge_stages) {
+        for (auto& row : rows[0]) {
+            std::vector<Deferred> merged;
+            merged.reserve(row.size());
+            std::vector<bool> used(row.size(), false);
+            for (size_t i = 0; i < row.size(); ++i) {
+                if (used[i])
+                    continue;
+                used[i] = true;
+                Deferred d = std::move(row[i]);
+                if (d.kind == kStage && d.ch.nrows == 1 && d.p.src.size() == 1 && d.p.dst.size() == 1) {
+                    const Ref s0 = d.p.src[0], d0 = d.p.dst[0];
+                    uint64_t ss = 0, ds = 0, n = 1;
+                    for (size_t j = i + 1; j < row.size(); ++j) {
+                        if (used[j])
+                            continue;
+                        const Deferred& e = row[j];
+                        if (e.kind != kStage || e.ch.nrows != 1 || e.ch.ncols != d.ch.ncols || e.p.src.size() != 1 ||
+                            e.p.dst.size() != 1 || e.p.src[0].buf != s0.buf || e.p.dst[0].buf != d0.buf)
+                            continue;
+                        const Ref& se = e.p.src[0];
+                        const Ref& de = e.p.dst[0];
+                        if (se.offset <= s0.offset || de.offset <= d0.offset)
+                            break;
+                        const uint64_t sse = (se.offset - s0.offset) / n, dse = (de.offset - d0.offset) / n;
+                        if (n == 1) {
+                            ss = sse;
+                            ds = dse;
+                        }
+                        if (sse != ss || dse != ds || ss * n != se.offset - s0.offset || ds * n != de.offset - d0.offset ||
+                            ss < d.ch.ncols || ds < d.ch.ncols)
+                            break;
+                        used[j] = true;
+                        ++n;
+                        for (const Sync& w : e.p.waits)
+                            d.p.waits.push_back(w);
+                        for (const Sync& q : e.p.posts)
+                            d.p.posts.push_back(q);
+                    }
+                    if (n > 1) {
+                        d.p.src[0].stride = ss;
+                        d.p.dst[0].stride = ds;
+                        d.ch = Chunk{0, n, 0, d.ch.ncols};
+                    }
+                }
+                merged.push_back(std::move(d));
+            }
+            row = std::move(merged);
+        }
+    }
+
     // Emit: producers of row t, their consumers L rows later, gathers of
     // reduced chunks one more lag later (or L when nothing sits between).
-    // The automatic lag puts about two grids of items between a producer and
-    // its first consumer, so consumers are claimed once producers are done.
+    // The automatic lag puts about two grids of producers between a producer
+    // and its first consumer, so consumers are claimed once producers are done.
+    // (Counting the consumers of a row too made the lag shorter and the
+    // composed AllReduce wait: 0.76 -> 0.49 of the roofline, measured.)
     if (lag < 0 && max_chunks > 0) {
         size_t per_row = std::max<size_t>(1, rows[0][0].size());
         // each CTA holds up to two claimed items, so about two grids of items

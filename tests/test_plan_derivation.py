@@ -299,3 +299,24 @@ def test_automatic_chunking_covers_every_element(kind, scale):
         assert sum(sizes[: len(sizes) // 4]) >= sum(sizes[-(len(sizes) // 4):])  # and ends with small ones
     outs = [np.zeros(len(w), NP[dtype]) for w in want]
     run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=3)
+
+
+def test_staged_stages_of_a_row_merge():
+    """In a staged plan, the stages one rank makes in one chunk row (its chunk of
+    every partition into consecutive ring slots) form one strided item, and the
+    plan still equals the oracle under the emulator."""
+    R, dtype = 4, "bf16"
+    n = 4 * 2048
+    ins = [rand(dtype, 60, r, n) for r in range(R)]
+    L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
+    pl = plan_for(L, L, "sum", dtype, R, policy(P.PL_PATH_STAGED, P.PL_AR_FUSED, chunk=1024), 64 * 1024)
+    st, items = plan_interp.load_plan(pl)
+    stages = [(it, refs) for it, refs, _ in items if it.kind == P.PL_ITEM_STAGE]
+    assert stages and all(it.rows == R for it, _ in stages)
+    for it, refs in stages:
+        src, dst = refs[0], refs[1]
+        assert src.stride == n // R and dst.space == P.PL_SPACE_SCRATCH and dst.stride >= it.cols
+        assert it.npost == R  # one notify per slot
+    want = oracle.allreduce(ins, dtype)
+    outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=5)
