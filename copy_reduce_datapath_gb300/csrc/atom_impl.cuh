@@ -1147,6 +1147,13 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u,
                 reinterpret_cast<unsigned long long*>(dyn) + kBulkMaxStages, 0u};
     const int tid = (int)threadIdx.x;
+    // With static claims the CTA's first item is blockIdx.x; when every item
+    // has refs_per_item references in order, each thread loads its reference
+    // of that item while thread 0 loads the header (one round trip less).
+    const bool early = !a.use_tickets && a.refs_per_item > 0 && blockIdx.x < a.nitems && tid < a.refs_per_item;
+    Ref r0{};
+    if (early)
+        r0 = a.refs[(size_t)blockIdx.x * (size_t)a.refs_per_item + (size_t)tid];
     if (tid == 0) {
         if (BULK) {
             for (int i = 0; i < stages; ++i)
@@ -1170,7 +1177,7 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     }
     __syncthreads();
     if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
-        put_ref<DT>(a, slot[0].item, a.refs[slot[0].item.ref + tid], sh[0], tid);
+        put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
     __syncthreads();
 
     if constexpr (ALIGN)

@@ -135,6 +135,7 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
     a.nbufs = 2 * R + 1;
     a.ops = wl.ops;
     a.all_aligned = wl.all_aligned;
+    a.refs_per_item = wl.refs_per_item;
     a.epoch = 1;  // the flags were zeroed above, so every call can use the same tags
     a.timeout_ns = 2000000000ull;
     a.drop_notify = -1;

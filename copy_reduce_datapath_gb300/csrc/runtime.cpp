@@ -389,6 +389,7 @@ struct HostPlan {
     int lag = 0;          // chunk rows between producers and their consumers in claim order
     int ops = 0;          // kOpsCopy | kOpsReduce, plus kOpsWide / kOpsMax
     int all_aligned = 0;  // every reference's byte offset and row stride is a multiple of 16
+    int refs_per_item = 0;  // n > 0: every item has n references, item i's at [i * n, i * n + n)
     pl_plan_stats stats{};
 };
 
@@ -1144,6 +1145,15 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     if (hp.items.size() >= (1ull << 31) || hp.refs.size() >= (1ull << 32) || hp.syncs.size() >= (1ull << 32))
         return PL_ERR_UNSUPPORTED;
     hp.nflags = staged ? (uint32_t)((uint64_t)R * slots_per_rank) : next_flag;
+    // Items with one reference count, laid out in order: a CTA that knows its
+    // first item's index loads that item's references alongside its header.
+    if (!hp.items.empty()) {
+        const uint32_t n = (uint32_t)hp.items[0].nsrc + hp.items[0].ndst;
+        bool uniform = n <= (uint32_t)kMaxRefsPerItem;
+        for (size_t i = 0; uniform && i < hp.items.size(); ++i)
+            uniform = (uint32_t)hp.items[i].nsrc + hp.items[i].ndst == n && hp.items[i].ref == (uint64_t)i * n;
+        hp.refs_per_item = uniform ? (int)n : 0;
+    }
     hp.all_aligned = 1;
     bool wide = true;
     for (const Item& it : hp.items) {
@@ -1668,6 +1678,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.nbufs = 2 * R + 1;
     a.ops = dp->hp.ops;
     a.all_aligned = dp->hp.all_aligned;
+    a.refs_per_item = dp->hp.refs_per_item;
     a.epoch = ++ctx->epoch;
     a.timeout_ns = rp.timeout_ns;
     a.drop_notify = rp.drop_notify;
@@ -1768,6 +1779,7 @@ int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bu
     out.nflags = hp.nflags;
     out.ops = hp.ops;
     out.all_aligned = hp.all_aligned;
+    out.refs_per_item = hp.refs_per_item;
     out.ctas = hp.stats.ctas;
     out.uses_tickets = hp.stats.uses_tickets;
     return PL_OK;

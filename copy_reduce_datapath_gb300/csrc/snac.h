@@ -100,6 +100,7 @@ struct LaunchArgs {
     int32_t nbufs;
     int32_t ops;                 // kOpsCopy | kOpsReduce present in the list, plus kOpsWide / kOpsMax
     int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
+    int32_t refs_per_item;       // n > 0: item i's references are refs[i * n .. i * n + n); 0: read the header
     unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
     unsigned long long timeout_ns;
     long long drop_notify;       // item index whose notifies are skipped, or -1
@@ -131,6 +132,7 @@ struct HostWorkList {
     uint32_t nflags = 0;
     int ops = 0;
     int all_aligned = 0;
+    int refs_per_item = 0;
     int ctas = 1;
     int uses_tickets = 0;
 };
