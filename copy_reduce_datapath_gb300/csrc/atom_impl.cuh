@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace purlin {
@@ -417,39 +418,22 @@ struct ItemShared {
 #define SRC_ROW(sh, s, row) ((sh).src[s] + (size_t)(row) * (sh).sstride[s])
 #define DST_ROW(sh, d, row) ((sh).dst[d] + (size_t)(row) * (sh).dstride[d])
 
-// Copy of nv 16-byte vectors from one source to every destination in `mask`.
-// The destinations are 16-byte aligned at `body`; the source is `q` bytes past
-// a 16-byte boundary (QALIGNED: q == 0).  U vectors in flight per thread.
-template <bool QALIGNED, int U>
+// Copy of nv 16-byte vectors from one source to every destination in `mask`,
+// both 16-byte aligned at `body` (the kernels for aligned plans).  U vectors
+// in flight per thread.
+template <int U>
 __device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
-                                       unsigned nv, int tid, int nthr)
+                                          unsigned nv, int tid, int nthr)
 {
     const char* src = SRC_ROW(sh, 0, row) + body;
-    const int q = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
-    const char* base = src - q;
     const unsigned step = (unsigned)nthr * U;
     for (unsigned v0 = tid; v0 < nv; v0 += step) {
         uint4 x[U];
-        if constexpr (QALIGNED) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                if (v < nv)
-                    x[u] = ld16(base + (size_t)v * 16);
-            }
-        } else {
-            uint4 lo[U], hi[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const unsigned v = v0 + u * nthr;
-                if (v < nv) {
-                    lo[u] = ld16(base + (size_t)v * 16);
-                    hi[u] = ld16(base + (size_t)v * 16 + 16);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                x[u] = realign(lo[u], hi[u], q);
+        for (int u = 0; u < U; ++u) {
+            const unsigned v = v0 + u * nthr;
+            if (v < nv)
+                x[u] = ld16(src + (size_t)v * 16);
         }
 #pragma unroll 1
         for (unsigned long long m = mask; m; m &= m - 1) {
@@ -465,13 +449,9 @@ __device__ __forceinline__ void copy_body(const ItemShared& sh, unsigned long lo
     }
 }
 
-// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
-// to every destination in `mask`.  G sources in flight per thread.
-// Rank-ordered fp32 sum of nsrc sources over nv vectors, rounded once, stored
-// to every destination in `mask`.  Aligned sources: U vectors x G sources
-// (U * G = 8 loads) in flight per thread, U chosen from the source count so
-// that few sources still keep the memory system busy.  Sources at mixed
-// misalignments (rare) are loaded one at a time and realigned.
+// Rank-ordered reduction (fp32 sum or maximum) of nsrc aligned sources over
+// nv vectors, rounded once, stored to every destination in `mask`: U vectors
+// x G sources (U * G = 8 loads) in flight per thread.
 template <int DT, bool MAXOP, int U>
 __device__ __forceinline__ void sum_aligned(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                             size_t body, unsigned nv, int tid, int nthr)
@@ -518,6 +498,9 @@ __device__ __forceinline__ void sum_aligned(const ItemShared& sh, int nsrc, unsi
     }
 }
 
+// The same reduction when the sources sit at different byte shifts from the
+// aligned destinations (rare): each source's 16 bytes are loaded as two
+// aligned vectors and realigned, one source at a time.
 template <int DT, bool MAXOP>
 __device__ __forceinline__ void sum_mixed(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                           size_t body, unsigned nv, int tid, int nthr)
@@ -897,7 +880,7 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
             if (tid == 0)
                 bulk_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body, nv * 16u, a);
         } else if constexpr (ALIGN) {
-            copy_body<true, kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
+            copy_body<kCopyUnroll>(sh, mask, row, body, nv, tid, nthr);
         } else if (BULK && nthr == (int)blockDim.x && bk.stages >= 4 && nv * 16u >= kBulkMin) {
             // a source misaligned against aligned destinations (q0 != 0 here)
             bulk_shift_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body - q0, q0, nv, tid, nthr, a);
@@ -1203,14 +1186,20 @@ cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_
 {
     size_t dyn = BULK ? 128 + (size_t)stages * kBulkPiece : 0;
     if (BULK) {
-        static bool configured = false;  // per instantiation; the attribute is per function
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(snac_kernel<DT, OPS, BULK, ALIGN>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)(128 + (size_t)kBulkMaxStages * kBulkPiece));
+        // The attribute belongs to the function in each device's context: one
+        // bit per device (of the first 64) once it is set there.
+        static std::atomic<unsigned long long> configured{0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+        if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+            e = cudaFuncSetAttribute(snac_kernel<DT, OPS, BULK, ALIGN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(128 + (size_t)kBulkMaxStages * kBulkPiece));
             if (e != cudaSuccess)
                 return e;
-            configured = true;
+            configured.fetch_or(bit, std::memory_order_acq_rel);
         }
     }
     snac_kernel<DT, OPS, BULK, ALIGN><<<ctas, ALIGN ? kThreads : kThreadsSpliced, dyn, stream>>>(args, stages);
