@@ -27,7 +27,8 @@ def ctx():
     P.pl_ctx_destroy(c)
 
 
-@pytest.mark.parametrize("dtype,R,n", [("bf16", 8, (1 << 20) + 77), ("fp32", 3, 3 * 4096), ("bf16", 5, 999)])
+@pytest.mark.parametrize("dtype,R,n", [("bf16", 8, (1 << 20) + 77), ("fp32", 3, 3 * 4096), ("bf16", 5, 999),
+                                       ("fp16", 8, (1 << 18) + 3)])
 def test_matches_allreduce_on_two_calls_in_a_row(ctx, dtype, R, n):
     s = P.stream_handle()
     calls = []
@@ -74,3 +75,4 @@ def test_rejects_sizes_beyond_its_limit():
     assert P.pl_allreduce_noalloc("bf16", 8, big, P.ptrs(x[:8]), P.ptrs(x[:8]), True, 0) == P.PL_ERR_NOMEM
     assert P.pl_allreduce_noalloc("bf16", 9, 8, P.ptrs(x), P.ptrs(x), True, 0) == P.PL_ERR_NOMEM
     assert P.pl_allreduce_noalloc("bf16", 2, 8, P.ptrs(x[:2]), P.ptrs(x[:2]), True, 0) == P.PL_OK
+    assert P.pl_allreduce_noalloc("fp8", 2, 8, P.ptrs(x[:2]), P.ptrs(x[:2]), True, 0) == P.PL_ERR_INVALID
