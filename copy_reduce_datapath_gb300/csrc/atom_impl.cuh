@@ -823,7 +823,7 @@ __device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int 
 template <int DT, int OPS, bool BULK, bool ALIGN>
 __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                         unsigned n, unsigned dcls, int tid, int nthr, BulkRing& bk,
-                                        const LaunchArgs& a)
+                                        const LaunchArgs& a, bool proven)
 {
     using EL = Elem<DT>;
     constexpr int S = EL::S;
@@ -835,7 +835,7 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
     if (head > n)
         head = n;
     unsigned nv = (n - head) / E;
-    if (ALIGN) {
+    if (ALIGN && !proven) {
         // Kernels built for plans the host proved 16-byte aligned have no
         // realigning bodies; should a segment still be misaligned, it is moved
         // element by element below (correct, slower).
@@ -869,12 +869,31 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         return;
 
     const size_t body = (size_t)head * S;
-    // Misalignment of every source relative to the aligned destinations.
-    const int q0 = (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, 0, row)) + body) & 15u);
+    // Misalignment of every source relative to the aligned destinations (none
+    // when the item's references are proven aligned).
+    int q0 = 0;
     bool uniform = true;
-    for (int s = 1; s < nsrc; ++s)
-        uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
+    if (!proven) {
+        q0 = (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, 0, row)) + body) & 15u);
+        for (int s = 1; s < nsrc; ++s)
+            uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
+    }
     const bool aligned = uniform && q0 == 0;
+    if (ALIGN && proven) {
+        // A small item: one thread per (vector, destination), so the item's
+        // stores issue at once instead of one destination after another (the
+        // bodies below take any thread count).  Proven items come with the
+        // destinations 0 .. nd-1 in one group.
+        const unsigned nd = (unsigned)__popcll(mask);
+        if (nd > 1 && nv * nd <= (unsigned)nthr) {
+            const unsigned d = (unsigned)tid / nv;
+            if (d >= nd)
+                return;
+            mask = 1ull << d;
+            tid -= (int)(d * nv);
+            nthr = (int)nv;
+        }
+    }
     if (COPY && (!REDUCE || nsrc == 1)) {
         if (BULK && aligned && nthr == (int)blockDim.x && nv * 16u >= kBulkMin) {
             if (tid == 0)
@@ -900,10 +919,13 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
 
 // Moves one rows x cols block.  A one-row block is spread over the whole CTA;
 // a multi-row block gives each warp whole rows.  Destinations are grouped by
-// address mod 16; each group is one pass over the sources.
+// address mod 16; each group is one pass over the sources.  `proven`: every
+// reference's row 0 and row stride are 16-byte aligned (checked per reference,
+// in parallel, when the references were loaded), so all destinations form one
+// group and no source needs realigning; the per-reference checks are skipped.
 template <int DT, int OPS, bool BULK, bool ALIGN>
 __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
-                                          unsigned long long cols, BulkRing& bk, const LaunchArgs& a)
+                                          unsigned long long cols, BulkRing& bk, const LaunchArgs& a, bool proven)
 {
     constexpr int S = Elem<DT>::S;
     constexpr bool COPY = (OPS & kOpsCopy) != 0;
@@ -912,9 +934,9 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
     if (rows > 1 && ((cols * S) & 15u) == 0) {
         // Rows of whole vectors, every row start aligned in every reference?
         bool flat = true;
-        for (int i = 0; i < nsrc; ++i)
+        for (int i = 0; !proven && i < nsrc; ++i)
             flat &= ((reinterpret_cast<uintptr_t>(sh.src[i]) | sh.sstride[i]) & 15u) == 0;
-        for (int i = 0; i < ndst; ++i)
+        for (int i = 0; !proven && i < ndst; ++i)
             flat &= ((reinterpret_cast<uintptr_t>(sh.dst[i]) | sh.dstride[i]) & 15u) == 0;
         if (flat) {
             const unsigned vpr = (unsigned)(cols * S / 16);
@@ -931,19 +953,24 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
     const int nthr = one_row ? (int)blockDim.x : 32;
     const unsigned r0 = one_row ? 0u : threadIdx.x >> 5;
     const unsigned rstep = one_row ? 1u : blockDim.x >> 5;
+    const unsigned long long all = ndst >= 64 ? ~0ull : ((1ull << ndst) - 1ull);
     for (unsigned r = r0; r < rows; r += rstep) {
-        unsigned long long todo = ndst >= 64 ? ~0ull : ((1ull << ndst) - 1ull);
+        unsigned long long todo = all;
         while (todo) {
-            const int d0 = __ffsll((long long)todo) - 1;
-            const unsigned cls = (unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d0, r)) & 15u);
-            unsigned long long group = 0;
-            for (unsigned long long m = todo; m; m &= m - 1) {
-                const int d = __ffsll((long long)m) - 1;
-                if ((unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d, r)) & 15u) == cls)
-                    group |= 1ull << d;
+            unsigned cls = 0;
+            unsigned long long group = todo;
+            if (!proven) {
+                const int d0 = __ffsll((long long)todo) - 1;
+                cls = (unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d0, r)) & 15u);
+                group = 0;
+                for (unsigned long long m = todo; m; m &= m - 1) {
+                    const int d = __ffsll((long long)m) - 1;
+                    if ((unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d, r)) & 15u) == cls)
+                        group |= 1ull << d;
+                }
             }
             todo &= ~group;
-            segment<DT, OPS, BULK, ALIGN>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a);
+            segment<DT, OPS, BULK, ALIGN>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a, proven);
         }
     }
 }
@@ -978,9 +1005,10 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* g)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Region pointer of reference `tid` of `it` into `sh`.
+// Region pointer of reference `tid` of `it` into `sh`.  Returns true when its
+// row 0 or its row stride is not a multiple of 16 bytes.
 template <int DT>
-__device__ __forceinline__ void put_ref(const LaunchArgs& a, const Item& it, const Ref& f, ItemShared& sh, int tid)
+__device__ __forceinline__ bool put_ref(const LaunchArgs& a, const Item& it, const Ref& f, ItemShared& sh, int tid)
 {
     constexpr int S = Elem<DT>::S;
     char* base = a.bufs[f.buf] + f.offset * (unsigned long long)S;
@@ -992,6 +1020,7 @@ __device__ __forceinline__ void put_ref(const LaunchArgs& a, const Item& it, con
         sh.dst[tid - it.nsrc] = base;
         sh.dstride[tid - it.nsrc] = stride;
     }
+    return ((reinterpret_cast<uintptr_t>(base) | stride) & 15u) != 0;
 }
 
 // Work-item loop of the kernels for aligned plans.  While item k moves, the
@@ -1001,7 +1030,7 @@ __device__ __forceinline__ void put_ref(const LaunchArgs& a, const Item& it, con
 // region pointers in two ItemShared buffers (items k, k+1).
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared* sh, Slot* slot, Ref* sref, int* s_ok,
-                                                BulkRing& bk, int tid)
+                                                BulkRing& bk, int tid, bool bad)
 {
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k % 3u), nxt = (int)((k + 1u) % 3u), nn = (int)((k + 2u) % 3u);
@@ -1041,19 +1070,21 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
             if (tid == 0)
                 *s_ok = ok ? 1 : 0;
         }
-        __syncthreads();
+        // `bad`: this thread's reference of item k is misaligned (put_ref)
+        const bool proven = !__syncthreads_or(bad);
         const bool ok = *s_ok != 0;  // read by every thread before the next write (after the barrier below)
         if (ok) {
             const Item& it = slot[cur].item;
-            move_item<DT, OPS, BULK, true>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a);
+            move_item<DT, OPS, BULK, true>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
         }
         cp_async_wait_all();
         __syncthreads();
+        bad = false;
         if (has_next) {
             // sh[snxt] served item k-1, whose move ended before the previous barrier
             const Item& nit = slot[nxt].item;
             if (tid < nit.nsrc + nit.ndst)
-                put_ref<DT>(a, nit, sref[tid], sh[snxt], tid);
+                bad = put_ref<DT>(a, nit, sref[tid], sh[snxt], tid);
         }
         if (tid < 32) {
             if (ok && slot[cur].item.npost)
@@ -1070,7 +1101,7 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
 // (which made the aligned kernels 1-3% faster).  Two header slots.
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* sh, Slot* slot, int* s_ok,
-                                               BulkRing& bk, int tid)
+                                               BulkRing& bk, int tid, bool bad)
 {
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k & 1u), nxt = cur ^ 1;
@@ -1096,12 +1127,14 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
             if (tid == 0)
                 *s_ok = ok ? 1 : 0;
         }
-        __syncthreads();
+        // `bad`: this thread's reference of item k is misaligned (put_ref)
+        const bool proven = !__syncthreads_or(bad);
         const bool ok = *s_ok != 0;
         if (ok)
-            move_item<DT, OPS, BULK, false>(sh[cur], it.nsrc, it.ndst, it.rows, it.cols, bk, a);
+            move_item<DT, OPS, BULK, false>(sh[cur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
+        bad = false;
         if (has_ref)
-            put_ref<DT>(a, nit, nref, sh[nxt], tid);  // sh[nxt] served item k-1, done before the last barrier
+            bad = put_ref<DT>(a, nit, nref, sh[nxt], tid);  // sh[nxt] served item k-1, done before the last barrier
         if (tid == 0) {
             // every thread read slot[cur] and slot[nxt] before the barrier above
             slot[cur].index = i2;
@@ -1159,14 +1192,14 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
         slot[1].item = h1;
     }
     __syncthreads();
+    bool bad = false;
     if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
-        put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
-    __syncthreads();
-
+        bad = put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
+    // The loops' first barrier publishes sh[0] before item 0 moves.
     if constexpr (ALIGN)
-        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid);
+        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad);
     else
-        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid);
+        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad);
 
     if (a.use_tickets && tid == 0) {
         __threadfence();
