@@ -1,7 +1,8 @@
-// Launch of the persistent SNAC kernel: picks the element type's
-// instantiation (this file holds the bf16 one; atom_fp16.cu, atom_fp32.cu and
-// atom_fp8.cu the others, compiled in parallel) and whether the plan may use
-// the kernels without realigning bodies.
+// Launches of the persistent SNAC kernel and of the inline-parameter kernel:
+// each picks the element type's instantiation (this file holds the bf16 ones;
+// atom_fp16.cu, atom_fp32.cu and atom_fp8.cu the others, compiled in
+// parallel), and the persistent kernel whether the plan may use the kernels
+// without realigning bodies.
 #include "atom_impl.cuh"
 
 namespace purlin {
@@ -9,6 +10,12 @@ namespace purlin {
 cudaError_t launch_snac_bf16(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s)
 {
     return launch_dtype<kDtBf16>(a, ctas, bulk, aligned, stages, s);
+}
+
+cudaError_t launch_inline_bf16(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                               cudaStream_t s)
+{
+    return launch_inline_dtype<kDtBf16>(maxop, small, large, nitems, s);
 }
 
 cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages, cudaStream_t stream)
@@ -29,6 +36,23 @@ cudaError_t launch_snac(const LaunchArgs& args, int ctas, bool bulk, int stages,
         return launch_snac_fp16(args, ctas, bulk, aligned, stages, stream);
     case kDtFp8:
         return launch_snac_fp8(args, ctas, bulk, aligned, stages, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_inline(int dtype, bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                          cudaStream_t stream)
+{
+    switch (dtype) {
+    case kDtBf16:
+        return launch_inline_bf16(maxop, small, large, nitems, stream);
+    case kDtFp32:
+        return launch_inline_fp32(maxop, small, large, nitems, stream);
+    case kDtFp16:
+        return launch_inline_fp16(maxop, small, large, nitems, stream);
+    case kDtFp8:
+        return launch_inline_fp8(maxop, small, large, nitems, stream);
     default:
         return cudaErrorInvalidValue;
     }

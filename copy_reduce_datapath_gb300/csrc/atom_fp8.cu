@@ -1,5 +1,5 @@
-// The one-byte (fp8) instantiation of the persistent SNAC kernel: copies only
-// (see atom_impl.cuh).
+// The one-byte (fp8) instantiations of the persistent SNAC kernel and of the
+// inline-parameter kernel: copies only (see atom_impl.cuh).
 #include "atom_impl.cuh"
 
 namespace purlin {
@@ -7,6 +7,12 @@ namespace purlin {
 cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s)
 {
     return launch_dtype<kDtFp8>(a, ctas, bulk, aligned, stages, s);
+}
+
+cudaError_t launch_inline_fp8(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                              cudaStream_t s)
+{
+    return launch_inline_dtype<kDtFp8>(maxop, small, large, nitems, s);
 }
 
 }  // namespace purlin

@@ -879,11 +879,13 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
             uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
     }
     const bool aligned = uniform && q0 == 0;
-    if (ALIGN && proven) {
+    if (ALIGN && proven && !a.no_spread) {
         // A small item: one thread per (vector, destination), so the item's
         // stores issue at once instead of one destination after another (the
         // bodies below take any thread count).  Proven items come with the
-        // destinations 0 .. nd-1 in one group.
+        // destinations 0 .. nd-1 in one group.  Not for a reduction in place,
+        // whose destinations include a source: there every vector is read
+        // whole by one thread before that thread writes it.
         const unsigned nd = (unsigned)__popcll(mask);
         if (nd > 1 && nv * nd <= (unsigned)nthr) {
             const unsigned d = (unsigned)tid / nv;
@@ -1269,6 +1271,165 @@ cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_
             return cudaErrorInvalidValue;
         }
     }
+}
+
+// ------------------------------------------------- inline-parameter kernel
+
+// The rank-ordered reduction (fp32 sum or maximum, rounded once) of vector
+// `off` of the nsrc sources p[0 ..], 8 loads in flight.
+template <int DT, bool MAXOP>
+__device__ __forceinline__ uint4 inline_reduce(char* const* p, unsigned ns, size_t off)
+{
+    Acc<DT, MAXOP> acc;
+    for (unsigned s0 = 0; s0 < ns; s0 += 8) {
+        uint4 x[8];
+#pragma unroll
+        for (unsigned q = 0; q < 8; ++q)
+            x[q] = s0 + q < ns ? ld16(p[s0 + q] + off) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (unsigned q = 0; q < 8; ++q) {
+            if (s0 + q < ns) {
+                if (s0 + q == 0)
+                    acc.set(x[q]);
+                else
+                    acc.add(x[q]);
+            }
+        }
+    }
+    return acc.pack();
+}
+
+// One item per CTA, read from the parameter block.  An item of at most one
+// vector per thread: each vector is read by g threads (g the CTA's threads per
+// vector, at most the item's destination count) and thread j of a vector
+// writes destinations j, j + g, j + 2g, ..., so the item's stores issue at
+// once.  A larger item: one thread per vector for every destination, U
+// vectors in flight per thread (a copy: U = 8; a reduction: 2 vectors x 8
+// sources per step), every source vector read once.  Then the last count
+// mod (16 / S) elements of each destination, element by element.  Reductions
+// combine the sources in rank order in fp32 (the sum or the maximum) and
+// round once, exactly as the persistent kernel does.  With
+// kInlineVectorWhole, g = 1: every vector is read whole by one thread before
+// it writes any destination (one of which may be one of its sources).
+template <int DT, bool MAXOP, int NI, int NP>
+__global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __grid_constant__ InlineArgs<NI, NP> a)
+{
+    using EL = Elem<DT>;
+    constexpr int S = EL::S;
+    constexpr unsigned E = 16 / S;
+    const InlineItem it = a.it[blockIdx.x];
+    char* const* p = a.ptr + it.ref;
+    const unsigned ns = it.nsrc, nd = it.ndst, n = it.count;
+    const unsigned nv = n / E, step = blockDim.x, tid = threadIdx.x;
+    const bool whole = (it.flags & kInlineVectorWhole) != 0;
+    const bool reduce = EL::kReducible && ns > 1;
+    if (nv > step) {
+        if (!reduce) {
+            constexpr int U = 8;
+            for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
+                uint4 x[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (v0 + u * step < nv)
+                        x[u] = ld16(p[0] + (size_t)(v0 + u * step) * 16);
+                for (unsigned d = 0; d < nd; ++d) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (v0 + u * step < nv)
+                            st16(p[1 + d] + (size_t)(v0 + u * step) * 16, x[u]);
+                }
+            }
+        } else if constexpr (EL::kReducible) {
+            constexpr int U = 2;
+            for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
+                Acc<DT, MAXOP> acc[U];
+                for (unsigned s0 = 0; s0 < ns; s0 += 8) {
+                    uint4 x[U][8];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const unsigned v = v0 + u * step;
+#pragma unroll
+                        for (unsigned q = 0; q < 8; ++q)
+                            x[u][q] = v < nv && s0 + q < ns ? ld16(p[s0 + q] + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+#pragma unroll
+                        for (unsigned q = 0; q < 8; ++q) {
+                            if (s0 + q < ns) {
+                                if (s0 + q == 0)
+                                    acc[u].set(x[u][q]);
+                                else
+                                    acc[u].add(x[u][q]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned v = v0 + u * step;
+                    if (v < nv) {
+                        const uint4 out = acc[u].pack();
+                        for (unsigned d = 0; d < nd; ++d)
+                            st16(p[ns + d] + (size_t)v * 16, out);
+                    }
+                }
+            }
+        }
+    } else if (nv > 0) {
+        const unsigned g = whole ? 1u : max(1u, min(nd, step / nv));
+        if (tid < nv * g) {
+            const unsigned j = tid / nv, v = tid - j * nv;
+            const size_t off = (size_t)v * 16;
+            uint4 out;
+            if constexpr (EL::kReducible) {
+                out = reduce ? inline_reduce<DT, MAXOP>(p, ns, off) : ld16(p[0] + off);
+            } else {
+                out = ld16(p[0] + off);
+            }
+            for (unsigned d = j; d < nd; d += g)
+                st16(p[ns + d] + off, out);
+        }
+    }
+    const unsigned t0 = nv * E, nt = n - t0;
+    const unsigned gt = whole || nt == 0 ? 1u : max(1u, min(nd, step / nt));
+    for (unsigned k = tid; k < nt * gt; k += step) {
+        const unsigned e = t0 + k % nt;
+        uint32_t x = EL::load(p[0] + (size_t)e * S);
+        if constexpr (EL::kReducible) {
+            if (ns > 1) {
+                float acc = EL::to_f(x);
+                for (unsigned q = 1; q < ns; ++q)
+                    acc = combine<MAXOP>(acc, EL::to_f(EL::load(p[q] + (size_t)e * S)));
+                x = EL::from_f(acc);
+            }
+        }
+        for (unsigned d = k / nt; d < nd; d += gt)
+            EL::store(p[ns + d] + (size_t)e * S, x);
+    }
+}
+
+template <int DT, bool MAXOP>
+cudaError_t launch_inline_op(const InlineSmall* small, const InlineLarge* large, int nitems, cudaStream_t stream)
+{
+    if (small)
+        snac_inline_kernel<DT, MAXOP, kInlineSmallItems, kInlineSmallPtrs><<<nitems, kInlineThreads, 0, stream>>>(*small);
+    else
+        snac_inline_kernel<DT, MAXOP, kInlineMaxItems, kInlineMaxPtrs><<<nitems, kInlineThreads, 0, stream>>>(*large);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_inline_dtype(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                                cudaStream_t stream)
+{
+    if (nitems < 1 || (small ? nitems > kInlineSmallItems : (!large || nitems > kInlineMaxItems)))
+        return cudaErrorInvalidValue;
+    if constexpr (Elem<DT>::kReducible) {
+        if (maxop)
+            return launch_inline_op<DT, true>(small, large, nitems, stream);
+    }
+    return launch_inline_op<DT, false>(small, large, nitems, stream);
 }
 
 template <int DT>

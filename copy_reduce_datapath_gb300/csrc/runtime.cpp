@@ -46,6 +46,14 @@ constexpr uint64_t kChunkGrain = 256;           // automatic chunk sizes are mul
 constexpr uint64_t kBulkItemBytes = 512 << 10;  // bytes (read + written) of an automatic bulk-ring item
 constexpr uint64_t kBulkChunkMin = 64 << 10;    // ... whose chunk stays within these
 constexpr uint64_t kBulkChunkMax = 256 << 10;
+// Inline-parameter plans (automatic): those whose every transfer reduces
+// several sources into one destination (the ReduceScatter shape, faster in
+// the inline kernel at every size measured, 1 KiB to 1 GiB), and others that
+// move at most this many bytes (measured crossovers on GB300, R = 8 bf16:
+// AllGather between 32 and 64 MiB per rank, 288 and 576 MiB moved; AllReduce
+// near 16 MiB per rank, 256 MiB moved; beyond them the persistent kernel's
+// bulk ring and pipelined items are faster).
+constexpr uint64_t kInlineAutoMoved = 320ull << 20;
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
@@ -341,7 +349,7 @@ struct Chunk {
 struct ResolvedPolicy {
     int path;       // PL_PATH_ZS / PL_PATH_STAGED
     int ar_form;    // PL_AR_FUSED / PL_AR_COMPOSED
-    int datapath;   // PL_ATOM_VECTOR / PL_ATOM_BULK
+    int datapath;   // PL_ATOM_VECTOR / PL_ATOM_BULK / PL_ATOM_INLINE
     bool datapath_auto;
     bool stages_auto;
     int ctas;       // 0 = auto
@@ -361,7 +369,7 @@ pl_status resolve_policy(const pl_policy* p, ResolvedPolicy& rp)
         return PL_ERR_INVALID;
     if (p->allreduce_form < PL_AR_AUTO || p->allreduce_form > PL_AR_COMPOSED)
         return PL_ERR_INVALID;
-    if (p->datapath < PL_ATOM_AUTO || p->datapath > PL_ATOM_BULK)
+    if (p->datapath < PL_ATOM_AUTO || p->datapath > PL_ATOM_INLINE)
         return PL_ERR_INVALID;
     if (p->ctas < 0 || p->stages < 0 || p->stages > kBulkMaxStages)
         return PL_ERR_INVALID;
@@ -390,6 +398,7 @@ struct HostPlan {
     int ops = 0;          // kOpsCopy | kOpsReduce, plus kOpsWide / kOpsMax
     int all_aligned = 0;  // every reference's byte offset and row stride is a multiple of 16
     int refs_per_item = 0;  // n > 0: every item has n references, item i's at [i * n, i * n + n)
+    bool inline_form = false;  // one-row aligned items that the inline-parameter kernel runs, one per CTA
     pl_plan_stats stats{};
 };
 
@@ -653,6 +662,22 @@ bool waits_precede(const HostPlan& hp)
 
 // Derives the work list with consumers emitted `lag` chunk rows behind the
 // producers they wait for (so the CTAs that claim them in order rarely spin).
+// Codesign policy for the datapath of the persistent kernel: large copy-only
+// plans stream through the bulk-copy ring (one shared-memory read per chunk,
+// one bulk store per destination) when their regions are 16-byte aligned, or
+// when they write at least twice what they read (a broadcast, the
+// AllGather(V) shape: misaligned sources are then realigned in shared memory
+// between the bulk load and the bulk stores); everything else uses the
+// vector datapath.  `hp.stats` holds the plan's bytes.
+bool launch_bulk(const HostPlan& hp, const ResolvedPolicy& pol)
+{
+    if (pol.datapath == PL_ATOM_BULK)
+        return true;
+    const pl_plan_stats& ps = hp.stats;
+    return pol.datapath_auto && hp.ops == kOpsCopy && (hp.all_aligned || ps.bytes_written >= 2 * ps.bytes_read) &&
+           ps.bytes_read + ps.bytes_written >= kBulkAutoBytes;
+}
+
 pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
                        const ResolvedPolicy& pol, int num_sms, Occupancy occ, uint64_t scratch_bytes, int lag,
                        HostPlan& hp)
@@ -785,7 +810,57 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
             equal &= t.count == ts[0].count && t.srcs.size() == ts[0].srcs.size() &&
                      t.dsts.size() == ts[0].dsts.size() && t.dsts[0].rows == 1;
         const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / fanout, kBulkChunkMin), kBulkChunkMax);
-        if (total_bytes / (uint64_t)full_grid <= kOneItemBytes) {
+        // Inline-parameter form (the whole plan in the launch's parameters, one
+        // item per CTA, no metadata loads): zero-staging one-row moves between
+        // 16-byte aligned regions, whose items and references fit the
+        // parameter block.  Each transfer gets its share of kInlineMaxItems
+        // items by bytes moved, in multiples of the grain.  Automatically: the
+        // ReduceScatter shape, or at most kInlineAutoMoved bytes moved.
+        std::vector<uint64_t> inline_target;
+        bool rs_shape = op != PL_COPY;
+        for (const Transfer& t : ts)
+            rs_shape &= t.srcs.size() > 1 && t.dsts.size() == 1;
+        const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && regions_aligned && moved > 0 &&
+                                 (pol.datapath == PL_ATOM_INLINE ||
+                                  (pol.datapath_auto && (rs_shape || moved <= kInlineAutoMoved)));
+        if (want_inline) {
+            bool fits = true;
+            uint64_t nitems = 0, nptrs = 0;
+            inline_target.assign(ts.size(), 0);
+            for (size_t i = 0; fits && i < ts.size(); ++i) {
+                const Transfer& t = ts[i];
+                for (const auto* side : {&t.srcs, &t.dsts})
+                    for (const Region& g : *side)
+                        fits &= g.rows == 1;
+                fits &= t.dsts.size() <= (size_t)kMaxRanks && t.srcs.size() <= (size_t)kMaxRanks;
+                if (!fits || t.count == 0)
+                    continue;
+                const uint64_t nref = t.srcs.size() + t.dsts.size();
+                const uint64_t share = std::max<uint64_t>(1, (uint64_t)kInlineMaxItems * (t.count * S * nref) / moved);
+                uint64_t target = (t.count + share - 1) / share;
+                target = (target + grain - 1) / grain * grain;
+                fits &= target * t.dsts.size() <= (1ull << 31);  // the kernel's 32-bit (vector, destination) index
+                inline_target[i] = target;
+                const uint64_t n = (t.count + target - 1) / target;
+                nitems += n;
+                nptrs += n * nref;
+            }
+            hp.inline_form = fits && nitems <= (uint64_t)kInlineMaxItems && nptrs <= (uint64_t)kInlineMaxPtrs;
+        }
+        if (hp.inline_form) {
+            for (size_t i = 0; i < ts.size(); ++i)
+                for (uint64_t left = ts[i].count; left > 0;) {
+                    const Chunk ch = next_chunk(ts[i], cur[i], inline_target[i], E);
+                    chunks[i].push_back(ch);
+                    left -= ch.nrows * ch.ncols;
+                }
+            for (auto& cs : chunks)
+                max_chunks = std::max(max_chunks, cs.size());
+            for (size_t c = 0; c < max_chunks; ++c)
+                for (size_t ti = 0; ti < ts.size(); ++ti)
+                    if (c < chunks[ti].size())
+                        order.push_back({ti, c});
+        } else if (total_bytes / (uint64_t)full_grid <= kOneItemBytes) {
             const uint64_t min_elems = round_grain(kMinChunkBytes / S);
             for (size_t i = 0; i < ts.size(); ++i) {
                 if (ts[i].count == 0)
@@ -1188,6 +1263,8 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     // needs no ticket.
     const bool claim_in_order = tickets || hp.items.size() > (size_t)ctas;
 
+    if (hp.inline_form && (hp.items.size() > (size_t)kInlineMaxItems || hp.refs.size() > (size_t)kInlineMaxPtrs))
+        hp.inline_form = false;  // (cannot happen: the cuts above are the items)
     pl_plan_stats& s = hp.stats;
     s.items = hp.items.size();
     s.refs = hp.refs.size();
@@ -1196,12 +1273,13 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     s.chunk_elems = chunk_elems;
     s.slots = slots_per_rank;
     s.slot_elems = staged ? slot_elems : 0;
-    s.ctas = ctas;
-    s.threads = kThreads;
-    s.uses_tickets = claim_in_order ? 1 : 0;
+    s.ctas = hp.inline_form ? (int)hp.items.size() : ctas;
+    s.threads = hp.inline_form ? kInlineThreads : kThreads;
+    s.uses_tickets = hp.inline_form ? 0 : (claim_in_order ? 1 : 0);
     s.path = pol.path;
     s.bytes_read = bytes_read;
     s.bytes_written = bytes_written;
+    s.datapath = hp.inline_form ? PL_ATOM_INLINE : launch_bulk(hp, pol) ? PL_ATOM_BULK : PL_ATOM_VECTOR;
     return PL_OK;
 }
 
@@ -1372,6 +1450,9 @@ struct pl_ctx {
     int last_cuda_error = 0;
     std::unordered_map<std::string, std::unique_ptr<DevicePlan>> cache;
     std::map<std::pair<int, uint64_t>, pl_layout*> ar_layouts;
+    // Host images of the inline kernel's parameter blocks (copied by each launch).
+    InlineSmall inline_small{};
+    std::unique_ptr<InlineLarge> inline_large = std::make_unique<InlineLarge>();
 };
 
 namespace {
@@ -1428,7 +1509,7 @@ std::string plan_key(const pl_layout& in, const pl_layout& out, pl_op op, pl_dty
 {
     uint64_t k[9] = {in.id, out.id, (uint64_t)op, (uint64_t)dt, (uint64_t)R, (uint64_t)rp.path,
                      (uint64_t)rp.ar_form,
-                     ((uint64_t)rp.ctas << 32) | ((uint64_t)rp.datapath_auto << 1) | (uint64_t)(rp.datapath == PL_ATOM_BULK),
+                     ((uint64_t)rp.ctas << 32) | ((uint64_t)rp.datapath_auto << 8) | (uint64_t)rp.datapath,
                      rp.chunk_bytes};
     return std::string(reinterpret_cast<const char*>(k), sizeof k);
 }
@@ -1479,12 +1560,15 @@ pl_status get_plan(pl_ctx* ctx, const pl_layout& in, const pl_layout& out, pl_op
     p->items = (const Item*)((char*)p->mem + oi);
     p->refs = (const Ref*)((char*)p->mem + orr);
     p->syncs = (const Sync*)((char*)p->mem + os);
-    // The device copy holds everything the kernel needs; keep host vectors only
-    // for stats.
-    p->hp.items.clear();
-    p->hp.items.shrink_to_fit();
-    p->hp.refs.clear();
-    p->hp.refs.shrink_to_fit();
+    // The device copy holds everything the persistent kernel needs; keep host
+    // vectors only for stats, and for the parameter block of an inline plan
+    // (at most kInlineMaxItems items and kInlineMaxPtrs references).
+    if (!p->hp.inline_form) {
+        p->hp.items.clear();
+        p->hp.items.shrink_to_fit();
+        p->hp.refs.clear();
+        p->hp.refs.shrink_to_fit();
+    }
     p->hp.syncs.clear();
     p->hp.syncs.shrink_to_fit();
     dp = p.get();
@@ -1503,8 +1587,10 @@ struct Interval {
 // rule: an output may only coincide exactly with one of its own sources.
 pl_status check_buffers(const pl_layout& in, const pl_layout& out, pl_dtype dt, int R,
                         void* const* in_bufs, const uint64_t* in_counts,
-                        void* const* out_bufs, const uint64_t* out_counts)
+                        void* const* out_bufs, const uint64_t* out_counts, bool* in_place = nullptr)
 {
+    if (in_place)
+        *in_place = false;
     const uint64_t S = elem_size(dt);
     std::vector<Interval> iv;
     for (int side = 0; side < 2; ++side) {
@@ -1544,6 +1630,8 @@ pl_status check_buffers(const pl_layout& in, const pl_layout& out, pl_dtype dt, 
                          (o.part->rows == 1 || o.part->row_stride == n.part->row_stride);
             if (!exact)
                 return PL_ERR_ALIAS;
+            if (in_place)
+                *in_place = true;
         }
     }
     return PL_OK;
@@ -1655,7 +1743,8 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     st = resolve_policy(policy, rp);
     if (st != PL_OK)
         return st;
-    if ((st = check_buffers(*in, *out, dt, R, in_bufs, in_counts, out_bufs, out_counts)) != PL_OK)
+    bool in_place = false;
+    if ((st = check_buffers(*in, *out, dt, R, in_bufs, in_counts, out_bufs, out_counts, &in_place)) != PL_OK)
         return st;
     DeviceGuard g(ctx->device);
     if (!g.ok())
@@ -1668,6 +1757,41 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         return PL_OK;  // nothing to move
     if ((st = ensure_flags(ctx, dp->hp.nflags)) != PL_OK)
         return st;
+    if (dp->hp.inline_form) {
+        // The whole plan in the launch's parameters, each reference resolved
+        // to its pointer; buffers that are not 16-byte aligned take the
+        // persistent kernel below (same items).
+        bool aligned = true;
+        for (int r = 0; r < R; ++r)
+            aligned &= ((reinterpret_cast<uintptr_t>(in_bufs[r]) | reinterpret_cast<uintptr_t>(out_bufs[r])) & 15u) == 0;
+        if (aligned) {
+            const int nitems = (int)dp->hp.items.size();
+            const bool small = nitems <= kInlineSmallItems && dp->hp.refs.size() <= (size_t)kInlineSmallPtrs;
+            InlineSmall* is = small ? &ctx->inline_small : nullptr;
+            InlineLarge* il = small ? nullptr : ctx->inline_large.get();
+            InlineItem* its = small ? is->it : il->it;
+            char** ptrs = small ? is->ptr : il->ptr;
+            const uint64_t S = elem_size(dt);
+            // In place, a reduction item's destinations include its own
+            // rank's source: each of its vectors is then read whole by one
+            // thread before that thread writes it anywhere.
+            for (int i = 0; i < nitems; ++i) {
+                const Item& it = dp->hp.items[i];
+                const bool whole = in_place && it.nsrc > 1 && it.ndst > 1;
+                its[i] = InlineItem{it.nsrc, it.ndst, it.ref, (uint32_t)it.cols, whole ? kInlineVectorWhole : 0u};
+            }
+            for (size_t k = 0; k < dp->hp.refs.size(); ++k) {
+                const Ref& f = dp->hp.refs[k];
+                char* base = f.buf < (uint32_t)R ? (char*)in_bufs[f.buf] : (char*)out_bufs[f.buf - R];
+                ptrs[k] = base + f.offset * S;
+            }
+            cudaError_t e = launch_inline(dt, (dp->hp.ops & kOpsMax) != 0, is, il, nitems, (cudaStream_t)stream);
+            if (e != cudaSuccess)
+                return cuda_fail(ctx, e);
+            ++ctx->launches;
+            return PL_OK;
+        }
+    }
     LaunchArgs a{};
     a.items = dp->items;
     a.refs = dp->refs;
@@ -1679,6 +1803,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.ops = dp->hp.ops;
     a.all_aligned = dp->hp.all_aligned;
     a.refs_per_item = dp->hp.refs_per_item;
+    a.no_spread = in_place && (dp->hp.ops & kOpsReduce) ? 1 : 0;
     a.epoch = ++ctx->epoch;
     a.timeout_ns = rp.timeout_ns;
     a.drop_notify = rp.drop_notify;
@@ -1688,22 +1813,10 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         a.bufs[R + r] = (char*)out_bufs[r];
     }
     a.bufs[2 * R] = ctx->scratch;
-    // Codesign policy for the datapath: large copy-only plans stream through
-    // the bulk-copy ring (one shared-memory read per chunk, one bulk store per
-    // destination) when their regions are 16-byte aligned, or when they write
-    // at least twice what they read (a broadcast, the AllGather(V) shape:
-    // misaligned sources are then realigned in shared memory between the
-    // bulk load and the bulk stores); everything else uses the vector
-    // datapath.
-    bool bulk = rp.datapath == PL_ATOM_BULK;
+    const bool bulk = launch_bulk(dp->hp, rp);
     int stages = rp.stages;
-    if (rp.datapath_auto && dp->hp.ops == kOpsCopy &&
-        (dp->hp.all_aligned || ps.bytes_written >= 2 * ps.bytes_read) &&
-        ps.bytes_read + ps.bytes_written >= kBulkAutoBytes) {
-        bulk = true;
-        if (rp.stages_auto)
-            stages = kBulkMaxStages;
-    }
+    if (bulk && rp.datapath_auto && rp.stages_auto)
+        stages = kBulkMaxStages;
     // The bulk ring's shared memory holds one CTA per SM: a grid sized for the
     // two-CTA spliced kernels is trimmed to one CTA per SM (claims adapt).
     const int ctas = bulk && !dp->hp.all_aligned ? std::min(ps.ctas, ctx->num_sms) : ps.ctas;

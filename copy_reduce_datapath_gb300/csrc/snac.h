@@ -101,6 +101,7 @@ struct LaunchArgs {
     int32_t ops;                 // kOpsCopy | kOpsReduce present in the list, plus kOpsWide / kOpsMax
     int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
     int32_t refs_per_item;       // n > 0: item i's references are refs[i * n .. i * n + n); 0: read the header
+    int32_t no_spread;           // 1: every vector is read and written by one thread (a reduction in place)
     unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
     unsigned long long timeout_ns;
     long long drop_notify;       // item index whose notifies are skipped, or -1
@@ -122,6 +123,56 @@ cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool align
 
 // CTAs of the SNAC kernel for aligned (or other) plans that fit on one SM at once.
 int snac_ctas_per_sm(bool aligned);
+
+// ------------------------------------------------- inline-parameter launches
+//
+// A small plan whose items are one-row moves between 16-byte aligned regions
+// travels whole in the kernel's parameters: one item per CTA, each reference
+// a resolved pointer, so the kernel starts moving data without loading any
+// metadata or waiting at a barrier.  Two sizes of parameter block: the small
+// one costs less per launch (measured on GB300: 2.3 KB blocks launch about
+// 0.2 us faster than 9-22 KB ones).
+constexpr int kInlineThreads = 512;
+constexpr int kInlineSmallItems = 16;
+constexpr int kInlineSmallPtrs = 256;
+constexpr int kInlineMaxItems = 152;
+constexpr int kInlineMaxPtrs = 2432;
+
+// One inline item: nsrc sources then ndst destinations at ptr[ref ..], count
+// elements each (copied when nsrc == 1, else reduced in source order).
+struct InlineItem {
+    uint16_t nsrc;
+    uint16_t ndst;
+    uint32_t ref;
+    uint32_t count;
+    uint32_t flags;  // kInlineVectorWhole
+};
+// The item's destinations include one of its sources (a reduction in place):
+// one thread reads each vector and writes it to every destination.
+constexpr uint32_t kInlineVectorWhole = 1;
+static_assert(sizeof(InlineItem) == 16, "InlineItem is 16 bytes");
+
+template <int NI, int NP>
+struct InlineArgs {
+    InlineItem it[NI];
+    char* ptr[NP];
+};
+using InlineSmall = InlineArgs<kInlineSmallItems, kInlineSmallPtrs>;
+using InlineLarge = InlineArgs<kInlineMaxItems, kInlineMaxPtrs>;
+static_assert(sizeof(InlineLarge) <= 32764, "kernel parameter limit");
+
+// Launch of an inline plan of `nitems` items (atom.cu): `small` selects the
+// parameter block; `maxop` the maximum instead of the sum for reductions.
+cudaError_t launch_inline(int dtype, bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                          cudaStream_t stream);
+cudaError_t launch_inline_bf16(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                               cudaStream_t s);
+cudaError_t launch_inline_fp16(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                               cudaStream_t s);
+cudaError_t launch_inline_fp32(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                               cudaStream_t s);
+cudaError_t launch_inline_fp8(bool maxop, const InlineSmall* small, const InlineLarge* large, int nitems,
+                              cudaStream_t s);
 
 // Host-side work list of a staged AllReduce whose device state lives in
 // caller-provided memory (runtime.cpp; used by the allocation-free entry point).

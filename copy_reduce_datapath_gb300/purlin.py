@@ -25,7 +25,7 @@ PL_COPY, PL_SUM, PL_MAX = 0, 1, 2
 PL_BF16, PL_FP32, PL_FP16, PL_FP8 = 0, 1, 2, 3
 PL_PATH_AUTO, PL_PATH_ZS, PL_PATH_STAGED = 0, 1, 2
 PL_AR_AUTO, PL_AR_FUSED, PL_AR_COMPOSED = 0, 1, 2
-PL_ATOM_AUTO, PL_ATOM_VECTOR, PL_ATOM_BULK = 0, 1, 2
+PL_ATOM_AUTO, PL_ATOM_VECTOR, PL_ATOM_BULK, PL_ATOM_INLINE = 0, 1, 2, 3
 PL_ITEM_MOVE, PL_ITEM_STAGE, PL_ITEM_CONSUME = 0, 1, 2
 PL_SPACE_IN, PL_SPACE_OUT, PL_SPACE_SCRATCH = 0, 1, 2
 PL_SYNC_WAIT_FULL, PL_SYNC_WAIT_FREE, PL_SYNC_NOTIFY, PL_SYNC_CREDIT = 0, 1, 2, 3
@@ -57,7 +57,8 @@ class pl_plan_stats(C.Structure):
                 ("flags", C.c_uint64), ("chunk_elems", C.c_uint64), ("slots", C.c_uint64),
                 ("slot_elems", C.c_uint64), ("ctas", C.c_int32), ("threads", C.c_int32),
                 ("uses_tickets", C.c_int32), ("path", C.c_int32),
-                ("bytes_read", C.c_uint64), ("bytes_written", C.c_uint64)]
+                ("bytes_read", C.c_uint64), ("bytes_written", C.c_uint64),
+                ("datapath", C.c_int32), ("reserved0", C.c_int32)]
 
 
 class pl_plan_item(C.Structure):

@@ -51,7 +51,7 @@ extern "C" {
 #define PL_API
 #endif
 
-#define PL_ABI_VERSION 1
+#define PL_ABI_VERSION 2
 
 /* ------------------------------------------------------------ status codes */
 
@@ -91,7 +91,7 @@ typedef int32_t pl_dtype;
 typedef struct pl_policy {
     int32_t path;            /* PL_PATH_AUTO / PL_PATH_ZS / PL_PATH_STAGED */
     int32_t allreduce_form;  /* PL_AR_AUTO / PL_AR_FUSED / PL_AR_COMPOSED (SUM with several outputs per name) */
-    int32_t datapath;        /* PL_ATOM_AUTO / PL_ATOM_VECTOR / PL_ATOM_BULK */
+    int32_t datapath;        /* PL_ATOM_AUTO / PL_ATOM_VECTOR / PL_ATOM_BULK / PL_ATOM_INLINE */
     int32_t ctas;            /* CTAs in the persistent grid; 0 = sized from the GPU's SM count and occupancy */
     int32_t stages;          /* depth of the bulk-copy shared-memory ring, 1..8; 0 = auto */
     int32_t reserved0;
@@ -109,13 +109,21 @@ typedef struct pl_policy {
 #define PL_AR_FUSED     1 /* one work item reduces a chunk and writes it to every output of its name */
 #define PL_AR_COMPOSED  2 /* Figure 6: the owner reduces its partition's chunk, notifies, the others gather it */
 
-#define PL_ATOM_AUTO    0 /* bulk ring (8 stages) for copy-only plans moving >= 64 MiB whose regions are 16-byte
+#define PL_ATOM_AUTO    0 /* inline for plans that qualify (below) and either move at most 320 MiB or reduce
+                             every name's sources into one destination (the ReduceScatter shape); else the bulk
+                             ring (8 stages) for copy-only plans moving >= 64 MiB whose regions are 16-byte
                              aligned or that write at least twice what they read; vector otherwise */
 #define PL_ATOM_VECTOR  1 /* 16-byte vector loads and stores by every thread */
 #define PL_ATOM_BULK    2 /* cp.async.bulk through a shared-memory ring for COPY work items: aligned sources
                              directly; sources at a byte shift from their destinations realigned in shared
                              memory between the bulk load and the bulk stores (4 stages or more); other
                              items use the vector datapath */
+#define PL_ATOM_INLINE  3 /* the whole work list in the kernel's launch parameters, one work item per CTA, every
+                             reference resolved to its pointer: no metadata loads, no barriers.  For zero-staging
+                             plans of one-row regions at 16-byte aligned offsets whose items (at most 152) and
+                             references (at most 2432) fit the parameter block.  Buffers not 16-byte aligned at
+                             launch, and plans that do not qualify, run the same work list on the vector (or bulk)
+                             datapath. */
 
 /* Fills *pol with the all-auto policy (debug_drop_notify = -1). */
 PL_API void pl_policy_default(pl_policy* pol);
@@ -288,6 +296,8 @@ typedef struct pl_plan_stats {
     int32_t path;          /* resolved PL_PATH_* */
     uint64_t bytes_read;   /* device bytes the plan reads per launch (algorithmic + staging) */
     uint64_t bytes_written;/* device bytes the plan writes per launch */
+    int32_t datapath;      /* resolved PL_ATOM_VECTOR / PL_ATOM_BULK / PL_ATOM_INLINE (for 16-byte aligned buffers) */
+    int32_t reserved0;
 } pl_plan_stats;
 
 /* Kinds of work items (SNAC steps). */

@@ -66,6 +66,12 @@ def assert_equal(got, want, what=""):
 # of 0xA5 would go unseen (1 in 256 per guard element).
 CANARY = {"bf16": 0x7FA5, "fp16": 0x7DA5, "fp32": 0x7FA5A5A5, "fp8": 0xA5}
 GUARD = 37  # elements of canary before and after every output
+SIZE = {"bf16": 2, "fp16": 2, "fp32": 4, "fp8": 1}
+
+
+def aligned_guard(dtype):
+    """Elements of a 64-byte canary: outputs after it keep the allocation's 16-byte alignment."""
+    return 64 // SIZE[dtype]
 
 
 def policies():
@@ -89,13 +95,16 @@ def ar_policies():
 
 
 class Outs:
-    """Output buffers with canary guard regions on both sides."""
+    """Output buffers with canary guard regions on both sides: `lead` elements
+    before each (GUARD by default, which leaves outputs off 16-byte alignment
+    for every element size) and GUARD after."""
 
-    def __init__(self, sizes, dtype):
+    def __init__(self, sizes, dtype, lead=GUARD):
         self.dtype = dtype
+        self.lead = int(lead)
         self.sizes = [int(s) for s in sizes]
-        self.full = [empty(s + 2 * GUARD, dtype, fill=CANARY[dtype]) for s in self.sizes]
-        self.views = [f[GUARD:GUARD + s] for f, s in zip(self.full, self.sizes)]
+        self.full = [empty(self.lead + s + GUARD, dtype, fill=CANARY[dtype]) for s in self.sizes]
+        self.views = [f[self.lead:self.lead + s] for f, s in zip(self.full, self.sizes)]
 
     def ptrs(self):
         from copy_reduce_datapath_gb300 import purlin as P
@@ -111,18 +120,29 @@ class Outs:
         canary = CANARY[self.dtype] & 0xFFFFFFFF
         for r, f in enumerate(self.full):
             b = bits(to_np(f, self.dtype))
-            assert np.all(b[:GUARD] == canary), f"rank {r}: write before its output"
-            assert np.all(b[GUARD + self.sizes[r]:] == canary), f"rank {r}: write past its output"
+            assert np.all(b[:self.lead] == canary), f"rank {r}: write before its output"
+            assert np.all(b[self.lead + self.sizes[r]:] == canary), f"rank {r}: write past its output"
 
 
 def run(ctx, lin, lout, op, dtype, ins_host, out_sizes, pol):
-    """One pl_collective over host inputs copied to the device; the outputs as host arrays."""
+    """pl_collective over host inputs copied to the device, twice: into outputs
+    at 16-byte aligned addresses (the kernels for aligned plans, the inline
+    form) and into outputs off that alignment (the realigning kernels).  Both
+    must agree bit for bit; the outputs as host arrays."""
     from copy_reduce_datapath_gb300 import purlin as P
     R = len(ins_host)
     ins = [to_dev(a, dtype) for a in ins_host]
-    outs = Outs(out_sizes, dtype)
     s = P.stream_handle()
-    P.pl_collective(ctx, lin, lout, op, dtype, R, P.ptrs(ins), P.counts(ins), outs.ptrs(), outs.counts(), pol, s)
-    assert P.pl_ctx_status(ctx, s) == P.PL_OK
-    outs.check_guards()
-    return [outs.host(r) for r in range(R)]
+    got = None
+    for lead in (aligned_guard(dtype), GUARD):
+        outs = Outs(out_sizes, dtype, lead)
+        P.pl_collective(ctx, lin, lout, op, dtype, R, P.ptrs(ins), P.counts(ins), outs.ptrs(), outs.counts(), pol, s)
+        assert P.pl_ctx_status(ctx, s) == P.PL_OK
+        outs.check_guards()
+        res = [outs.host(r) for r in range(R)]
+        if got is None:
+            got = res
+        else:
+            for r in range(R):
+                assert_equal(res[r], got[r], f"misaligned outputs, rank {r}")
+    return got

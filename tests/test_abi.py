@@ -42,7 +42,7 @@ def test_exports_are_only_the_abi(libpath):
 
 def test_abi_version_and_status_strings(libpath):
     from copy_reduce_datapath_gb300 import purlin as P
-    assert P.pl_abi_version() == 1
+    assert P.pl_abi_version() == 2
     for st in range(8):
         assert P.pl_status_str(st) and P.pl_status_str(st) != "unknown status"
     assert P.pl_status_str(99) == "unknown status"

@@ -320,3 +320,103 @@ def test_staged_stages_of_a_row_merge():
     want = oracle.allreduce(ins, dtype)
     outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=5)
+
+
+# ------------------------------------------------ the inline-parameter form
+
+
+def small_layouts(coll, R, n):
+    """Layout pair and op of an equal-partition collective over n elements per rank."""
+    lens = [n // R] * R
+    if coll == "allgather":
+        return P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy"
+    if coll == "reducescatter":
+        return P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), "sum"
+    L = P.pl_layout_partitioned(R, lens)
+    return L, L, "sum"
+
+
+def oracle_of(coll, ins, R, n, dtype):
+    if coll == "allgather":
+        return oracle.allgather(ins, dtype)
+    if coll == "reducescatter":
+        return oracle.reducescatter(ins, [n // R] * R, dtype)
+    return oracle.allreduce(ins, dtype)
+
+
+@pytest.mark.parametrize("T", [1 << 10, 1 << 13, 1 << 16, 1 << 18])
+@pytest.mark.parametrize("coll", ["allgather", "allreduce", "reducescatter"])
+def test_inline_form_for_small_aligned_plans(coll, T):
+    """Zero-staging one-row plans between 16-byte aligned regions, small enough:
+    the whole list in the launch parameters, one item per CTA (at most 152
+    items, 2432 references); a 1 KiB message fits the small parameter block.
+    Executed by the emulator, the result equals the oracle."""
+    R, dtype = 8, "bf16"
+    n = T // 2
+    lin, lout, op = small_layouts(coll, R, n)
+    pl = P.pl_plan_create(lin, lout, op, dtype, R, None, num_sms=152)
+    st, items = plan_interp.load_plan(pl)
+    assert st.datapath == P.PL_ATOM_INLINE
+    assert st.ctas == st.items <= 152 and st.refs <= 2432 and st.threads == 512 and st.uses_tickets == 0
+    if T == 1 << 10:
+        assert st.items <= 16 and st.refs <= 256
+    for it, refs, syncs in items:
+        assert it.rows == 1 and not syncs and it.kind == P.PL_ITEM_MOVE
+        assert all(f.offset * 2 % 16 == 0 for f in refs)
+    in_n = n // R if coll == "allgather" else n
+    ins = [rand(dtype, 70, r, in_n) for r in range(R)]
+    want = oracle_of(coll, ins, R, n, dtype)
+    outs = [np.zeros(len(w), NP[dtype]) for w in want]
+    run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=7)
+
+
+def test_inline_form_not_taken():
+    """Plans the inline form does not take: moving more than 320 MiB (unless
+    every transfer reduces into one destination), staged, composed, strided,
+    misaligned, a fixed grid, a forced datapath, too many references; the form
+    forced on a plan it cannot take leaves the vector datapath."""
+    R, dtype, n = 8, "bf16", 1 << 12
+
+    def form(lin, lout, op, pol=None, R_=R):
+        pl = P.pl_plan_create(lin, lout, op, dtype, R_, pol, num_sms=152, scratch_bytes=1 << 20)
+        try:
+            return P.pl_plan_get_stats(pl).datapath
+        finally:
+            P.pl_plan_destroy(pl)
+
+    ag = small_layouts("allgather", R, n)
+    ar = small_layouts("allreduce", R, n)
+    assert form(*ag) == P.PL_ATOM_INLINE and form(*ar) == P.PL_ATOM_INLINE
+    assert form(*small_layouts("allgather", R, 1 << 23)) == P.PL_ATOM_INLINE        # 16 MiB per rank: 144 MiB moved
+    assert form(*small_layouts("allgather", R, 1 << 25)) == P.PL_ATOM_BULK          # 64 MiB: the bulk ring
+    assert form(*small_layouts("allreduce", R, 1 << 23)) == P.PL_ATOM_INLINE        # 256 MiB moved
+    assert form(*small_layouts("allreduce", R, 1 << 24)) == P.PL_ATOM_VECTOR        # 512 MiB moved
+    assert form(*small_layouts("reducescatter", R, 1 << 29)) == P.PL_ATOM_INLINE    # 1 GiB: the ReduceScatter shape
+    assert form(*ag, P.pl_policy_default(path=P.PL_PATH_STAGED)) == P.PL_ATOM_VECTOR
+    assert form(*ar, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED)) == P.PL_ATOM_VECTOR
+    assert form(*ag, P.pl_policy_default(ctas=64)) == P.PL_ATOM_VECTOR
+    assert form(*ag, P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)) == P.PL_ATOM_VECTOR
+    assert form(*ag, P.pl_policy_default(datapath=P.PL_ATOM_BULK)) == P.PL_ATOM_BULK
+    assert form(*ag, P.pl_policy_default(chunk_bytes=1024)) == P.PL_ATOM_VECTOR
+    uly = (P.pl_layout_ulysses_in(R, 16, 16, 8), P.pl_layout_ulysses_out(R, 16, 16, 8), "copy")
+    assert form(*uly) == P.PL_ATOM_VECTOR
+    assert form(*uly, P.pl_policy_default(datapath=P.PL_ATOM_INLINE)) == P.PL_ATOM_VECTOR
+    lens = synth.zipf_lengths(3001, R, 0.125, seed=71)
+    assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_VECTOR
+    L64 = P.pl_layout_partitioned(64, [64] * 64)
+    assert form(L64, L64, "sum", None, 64) == P.PL_ATOM_VECTOR                     # 64 x 128 references
+
+
+def test_forced_inline_cuts_at_most_152_items():
+    """PL_ATOM_INLINE forced on a 2 MiB AllGather: at most 152 items, as large
+    as the message needs; the emulator gives the oracle's result."""
+    R, dtype, n = 8, "bf16", (1 << 20) + 8 * 16
+    lin, lout, op = small_layouts("allgather", R, n)
+    pl = P.pl_plan_create(lin, lout, op, dtype, R, P.pl_policy_default(datapath=P.PL_ATOM_INLINE), num_sms=152)
+    st, items = plan_interp.load_plan(pl)
+    assert st.datapath == P.PL_ATOM_INLINE and st.items <= 152
+    assert sum(it.cols for it, _, _ in items) == n
+    ins = [rand(dtype, 72, r, n // R) for r in range(R)]
+    want = oracle.allgather(ins, dtype)
+    outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window=16, seed=9)
