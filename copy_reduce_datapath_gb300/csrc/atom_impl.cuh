@@ -1275,40 +1275,61 @@ cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_
 
 // ------------------------------------------------- inline-parameter kernel
 
-// The rank-ordered reduction (fp32 sum or maximum, rounded once) of vector
-// `off` of the nsrc sources p[0 ..], 8 loads in flight.
-template <int DT, bool MAXOP>
+// The rank-ordered reduction (fp32 sum or maximum, rounded once) of the 16
+// bytes at byte offset `off` of the ns sources p[0 ..], 8 sources in flight.
+// ALIGNED: every source address is 16-byte aligned.  Otherwise a source at a
+// byte shift q is read as the two aligned vectors around it (every load of
+// the 8 sources is issued before any splice) and spliced; the aligned vector
+// holding its last byte, which belongs to the region, is the second, so no
+// load leaves the buffer.
+template <int DT, bool MAXOP, bool ALIGNED>
 __device__ __forceinline__ uint4 inline_reduce(char* const* p, unsigned ns, size_t off)
 {
     Acc<DT, MAXOP> acc;
     for (unsigned s0 = 0; s0 < ns; s0 += 8) {
-        uint4 x[8];
+        uint4 lo[8], hi[8];
+        int sh[8];
 #pragma unroll
-        for (unsigned q = 0; q < 8; ++q)
-            x[q] = s0 + q < ns ? ld16(p[s0 + q] + off) : make_uint4(0, 0, 0, 0);
+        for (unsigned q = 0; q < 8; ++q) {
+            const char* a = s0 + q < ns ? p[s0 + q] + off : p[0] + off;
+            sh[q] = ALIGNED ? 0 : (int)(reinterpret_cast<uintptr_t>(a) & 15u);
+            lo[q] = s0 + q < ns ? ld16(a - sh[q]) : make_uint4(0, 0, 0, 0);
+            hi[q] = !ALIGNED && s0 + q < ns && sh[q] ? ld16(a - sh[q] + 16) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (unsigned q = 0; q < 8; ++q) {
             if (s0 + q < ns) {
+                const uint4 x = !ALIGNED && sh[q] ? realign(lo[q], hi[q], sh[q]) : lo[q];
                 if (s0 + q == 0)
-                    acc.set(x[q]);
+                    acc.set(x);
                 else
-                    acc.add(x[q]);
+                    acc.add(x);
             }
         }
     }
     return acc.pack();
 }
 
-// One item per CTA, read from the parameter block.  An item of at most one
-// vector per thread: each vector is read by g threads (g the CTA's threads per
-// vector, at most the item's destination count) and thread j of a vector
-// writes destinations j, j + g, j + 2g, ..., so the item's stores issue at
-// once.  A larger item: one thread per vector for every destination, U
-// vectors in flight per thread (a copy: U = 8; a reduction: 2 vectors x 8
-// sources per step), every source vector read once.  Then the last count
-// mod (16 / S) elements of each destination, element by element.  Reductions
-// combine the sources in rank order in fp32 (the sum or the maximum) and
-// round once, exactly as the persistent kernel does.  With
+// One item per CTA, read from the parameter block.
+//  - An item whose every pointer is 16-byte aligned (kInlineAligned, from
+//    the host) of at most one vector per thread: each vector is read by g
+//    threads (g the CTA's threads per vector, at most the item's destination
+//    count) and thread j of a vector writes destinations j, j + g, j + 2g,
+//    ..., so the item's stores issue at once.  A larger one: one thread per
+//    vector for every destination, U vectors in flight per thread (a copy:
+//    U = 8; a reduction: 2 vectors x 8 sources per step), every source
+//    vector read once.
+//  - Another item: its destinations share their address mod 16 (the host
+//    checks it; should they not, the whole item moves element by element).
+//    The body between the destinations' first and last 16-byte boundaries
+//    moves in vectors as above (g threads per vector, looping with g = 1 when
+//    larger: copies 4 vectors in flight per thread, reductions 8 sources); a
+//    source at another byte shift is read as the two aligned vectors around
+//    each of its vectors and spliced.
+//  - The elements before the body (the head) and after it (the tail) move one
+//    (element, destination) pair per thread.
+// Reductions combine the sources in rank order in fp32 (the sum or the
+// maximum) and round once, exactly as the persistent kernel does.  With
 // kInlineVectorWhole, g = 1: every vector is read whole by one thread before
 // it writes any destination (one of which may be one of its sources).
 template <int DT, bool MAXOP, int NI, int NP>
@@ -1319,92 +1340,149 @@ __global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __
     constexpr unsigned E = 16 / S;
     const InlineItem it = a.it[blockIdx.x];
     char* const* p = a.ptr + it.ref;
-    const unsigned ns = it.nsrc, nd = it.ndst, n = it.count;
-    const unsigned nv = n / E, step = blockDim.x, tid = threadIdx.x;
+    const unsigned ns = it.nsrc, nd = it.ndst, n = it.count, step = blockDim.x, tid = threadIdx.x;
     const bool whole = (it.flags & kInlineVectorWhole) != 0;
     const bool reduce = EL::kReducible && ns > 1;
-    if (nv > step) {
-        if (!reduce) {
-            constexpr int U = 8;
-            for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
-                uint4 x[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (v0 + u * step < nv)
-                        x[u] = ld16(p[0] + (size_t)(v0 + u * step) * 16);
-                for (unsigned d = 0; d < nd; ++d) {
+    unsigned h = 0, nv = n / E;
+    if (it.flags & kInlineAligned) {
+        if (nv > step) {
+            if (!reduce) {
+                constexpr int U = 8;
+                for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
+                    uint4 x[U];
 #pragma unroll
                     for (int u = 0; u < U; ++u)
                         if (v0 + u * step < nv)
-                            st16(p[1 + d] + (size_t)(v0 + u * step) * 16, x[u]);
-                }
-            }
-        } else if constexpr (EL::kReducible) {
-            constexpr int U = 2;
-            for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
-                Acc<DT, MAXOP> acc[U];
-                for (unsigned s0 = 0; s0 < ns; s0 += 8) {
-                    uint4 x[U][8];
+                            x[u] = ld16(p[0] + (size_t)(v0 + u * step) * 16);
+                    for (unsigned d = 0; d < nd; ++d) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const unsigned v = v0 + u * step;
-#pragma unroll
-                        for (unsigned q = 0; q < 8; ++q)
-                            x[u][q] = v < nv && s0 + q < ns ? ld16(p[s0 + q] + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+                        for (int u = 0; u < U; ++u)
+                            if (v0 + u * step < nv)
+                                st16(p[1 + d] + (size_t)(v0 + u * step) * 16, x[u]);
                     }
+                }
+            } else if constexpr (EL::kReducible) {
+                constexpr int U = 2;
+                for (unsigned v0 = tid; v0 < nv; v0 += U * step) {
+                    Acc<DT, MAXOP> acc[U];
+                    for (unsigned s0 = 0; s0 < ns; s0 += 8) {
+                        uint4 x[U][8];
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
+                        for (int u = 0; u < U; ++u) {
+                            const unsigned v = v0 + u * step;
 #pragma unroll
-                        for (unsigned q = 0; q < 8; ++q) {
-                            if (s0 + q < ns) {
-                                if (s0 + q == 0)
-                                    acc[u].set(x[u][q]);
-                                else
-                                    acc[u].add(x[u][q]);
+                            for (unsigned q = 0; q < 8; ++q)
+                                x[u][q] = v < nv && s0 + q < ns ? ld16(p[s0 + q] + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+#pragma unroll
+                            for (unsigned q = 0; q < 8; ++q) {
+                                if (s0 + q < ns) {
+                                    if (s0 + q == 0)
+                                        acc[u].set(x[u][q]);
+                                    else
+                                        acc[u].add(x[u][q]);
+                                }
                             }
                         }
                     }
-                }
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const unsigned v = v0 + u * step;
-                    if (v < nv) {
-                        const uint4 out = acc[u].pack();
-                        for (unsigned d = 0; d < nd; ++d)
-                            st16(p[ns + d] + (size_t)v * 16, out);
+                    for (int u = 0; u < U; ++u) {
+                        const unsigned v = v0 + u * step;
+                        if (v < nv) {
+                            const uint4 out = acc[u].pack();
+                            for (unsigned d = 0; d < nd; ++d)
+                                st16(p[ns + d] + (size_t)v * 16, out);
+                        }
                     }
                 }
             }
-        }
-    } else if (nv > 0) {
-        const unsigned g = whole ? 1u : max(1u, min(nd, step / nv));
-        if (tid < nv * g) {
-            const unsigned j = tid / nv, v = tid - j * nv;
-            const size_t off = (size_t)v * 16;
-            uint4 out;
-            if constexpr (EL::kReducible) {
-                out = reduce ? inline_reduce<DT, MAXOP>(p, ns, off) : ld16(p[0] + off);
-            } else {
-                out = ld16(p[0] + off);
+        } else if (nv > 0) {
+            const unsigned g = whole ? 1u : max(1u, min(nd, step / nv));
+            if (tid < nv * g) {
+                const unsigned j = tid / nv, v = tid - j * nv;
+                const size_t off = (size_t)v * 16;
+                uint4 out;
+                if constexpr (EL::kReducible)
+                    out = reduce ? inline_reduce<DT, MAXOP, true>(p, ns, off) : ld16(p[0] + off);
+                else
+                    out = ld16(p[0] + off);
+                for (unsigned d = j; d < nd; d += g)
+                    st16(p[ns + d] + off, out);
             }
-            for (unsigned d = j; d < nd; d += g)
-                st16(p[ns + d] + off, out);
+        }
+    } else {
+        const unsigned dcls = (unsigned)(reinterpret_cast<uintptr_t>(p[ns]) & 15u);
+        bool congruent = true;
+        for (unsigned d = 1; d < nd; ++d)
+            congruent &= (unsigned)(reinterpret_cast<uintptr_t>(p[ns + d]) & 15u) == dcls;
+        h = congruent ? min(n, ((16u - dcls) & 15u) / S) : n;
+        nv = (n - h) / E;
+        const size_t body = (size_t)h * S;
+        const unsigned g = whole || nv > step ? 1u : max(1u, min(nd, step / max(nv, 1u)));
+        const unsigned total = nv * g;
+        if (!reduce) {
+            // one source at shift q: its aligned vectors, loaded before any splice
+            constexpr int U = 4;
+            const int q = (int)((reinterpret_cast<uintptr_t>(p[0]) + body) & 15u);
+            const char* src = p[0] + body - q;
+            for (unsigned k0 = tid; k0 < total; k0 += U * step) {
+                uint4 lo[U], hi[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned k = k0 + u * step;
+                    const size_t at = (size_t)(k % nv) * 16;
+                    lo[u] = k < total ? ld16(src + at) : make_uint4(0, 0, 0, 0);
+                    hi[u] = k < total && q ? ld16(src + at + 16) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned k = k0 + u * step;
+                    if (k < total) {
+                        const uint4 x = q ? realign(lo[u], hi[u], q) : lo[u];
+                        const size_t off = body + (size_t)(k % nv) * 16;
+                        for (unsigned d = k / nv; d < nd; d += g)
+                            st16(p[1 + d] + off, x);
+                    }
+                }
+            }
+        } else if constexpr (EL::kReducible) {
+            for (unsigned k = tid; k < total; k += step) {
+                const unsigned j = k / nv, v = k - j * nv;
+                const size_t off = body + (size_t)v * 16;
+                const uint4 out = inline_reduce<DT, MAXOP, false>(p, ns, off);
+                for (unsigned d = j; d < nd; d += g)
+                    st16(p[ns + d] + off, out);
+            }
         }
     }
-    const unsigned t0 = nv * E, nt = n - t0;
-    const unsigned gt = whole || nt == 0 ? 1u : max(1u, min(nd, step / nt));
-    for (unsigned k = tid; k < nt * gt; k += step) {
-        const unsigned e = t0 + k % nt;
+    // head [0, h) and tail [h + nv * E, n), one element each
+    const unsigned t0 = h + nv * E, ne = h + (n - t0);
+    if (ne == 0)
+        return;
+    const unsigned gt = whole ? 1u : max(1u, min(nd, step / ne));
+    for (unsigned k = tid; k < ne * gt; k += step) {
+        const unsigned i = k % ne, e = i < h ? i : t0 + (i - h);
         uint32_t x = EL::load(p[0] + (size_t)e * S);
         if constexpr (EL::kReducible) {
             if (ns > 1) {
+                // sources 8 at a time in flight, folded in rank order
                 float acc = EL::to_f(x);
-                for (unsigned q = 1; q < ns; ++q)
-                    acc = combine<MAXOP>(acc, EL::to_f(EL::load(p[q] + (size_t)e * S)));
+                for (unsigned s0 = 1; s0 < ns; s0 += 8) {
+                    uint32_t y[8];
+#pragma unroll
+                    for (unsigned q = 0; q < 8; ++q)
+                        y[q] = s0 + q < ns ? EL::load(p[s0 + q] + (size_t)e * S) : 0u;
+#pragma unroll
+                    for (unsigned q = 0; q < 8; ++q)
+                        if (s0 + q < ns)
+                            acc = combine<MAXOP>(acc, EL::to_f(y[q]));
+                }
                 x = EL::from_f(acc);
             }
         }
-        for (unsigned d = k / nt; d < nd; d += gt)
+        for (unsigned d = k / ne; d < nd; d += gt)
             EL::store(p[ns + d] + (size_t)e * S, x);
     }
 }

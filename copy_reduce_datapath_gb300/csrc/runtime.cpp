@@ -54,6 +54,13 @@ constexpr uint64_t kBulkChunkMax = 256 << 10;
 // near 16 MiB per rank, 256 MiB moved; beyond them the persistent kernel's
 // bulk ring and pipelined items are faster).
 constexpr uint64_t kInlineAutoMoved = 320ull << 20;
+// Inline items over regions not all 16-byte aligned: at most this many body
+// vectors, which the kernel's realigning loop moves: four per thread for a
+// copy, two for a reduction (its loop holds one vector of 8 sources at a
+// time; with four a ReduceScatterV of 4 MiB per rank ran 12.0 us against the
+// persistent kernel's 10.5).
+constexpr uint64_t kInlineMisalignedCopyVectors = 4 * kInlineThreads;
+constexpr uint64_t kInlineMisalignedReduceVectors = 2 * kInlineThreads;
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
@@ -398,7 +405,8 @@ struct HostPlan {
     int ops = 0;          // kOpsCopy | kOpsReduce, plus kOpsWide / kOpsMax
     int all_aligned = 0;  // every reference's byte offset and row stride is a multiple of 16
     int refs_per_item = 0;  // n > 0: every item has n references, item i's at [i * n, i * n + n)
-    bool inline_form = false;  // one-row aligned items that the inline-parameter kernel runs, one per CTA
+    bool inline_form = false;  // one-row items that the inline-parameter kernel runs, one per CTA
+    bool inline_any_alignment = false;  // ... over buffers at any alignment (small items)
     pl_plan_stats stats{};
 };
 
@@ -811,18 +819,23 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                      t.dsts.size() == ts[0].dsts.size() && t.dsts[0].rows == 1;
         const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / fanout, kBulkChunkMin), kBulkChunkMax);
         // Inline-parameter form (the whole plan in the launch's parameters, one
-        // item per CTA, no metadata loads): zero-staging one-row moves between
-        // 16-byte aligned regions, whose items and references fit the
-        // parameter block.  Each transfer gets its share of kInlineMaxItems
-        // items by bytes moved, in multiples of the grain.  Automatically: the
-        // ReduceScatter shape, or at most kInlineAutoMoved bytes moved.
+        // item per CTA, no metadata loads): zero-staging one-row moves whose
+        // items and references fit the parameter block, every transfer's
+        // destinations at one offset mod 16 bytes.  Each transfer gets its
+        // share of kInlineMaxItems items by bytes moved, in multiples of the
+        // grain.  Regions not all 16-byte aligned: items of at most
+        // kInlineMisalignedCopyVectors (copies) or kInlineMisalignedReduceVectors
+        // (reductions) vectors (the kernel's fastest loop, for larger items,
+        // wants aligned references).  Automatically: the
+        // ReduceScatter shape between aligned regions, or at most
+        // kInlineAutoMoved bytes moved.
         std::vector<uint64_t> inline_target;
         bool rs_shape = op != PL_COPY;
         for (const Transfer& t : ts)
             rs_shape &= t.srcs.size() > 1 && t.dsts.size() == 1;
-        const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && regions_aligned && moved > 0 &&
+        const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && moved > 0 &&
                                  (pol.datapath == PL_ATOM_INLINE ||
-                                  (pol.datapath_auto && (rs_shape || moved <= kInlineAutoMoved)));
+                                  (pol.datapath_auto && ((rs_shape && regions_aligned) || moved <= kInlineAutoMoved)));
         if (want_inline) {
             bool fits = true;
             uint64_t nitems = 0, nptrs = 0;
@@ -832,6 +845,8 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                 for (const auto* side : {&t.srcs, &t.dsts})
                     for (const Region& g : *side)
                         fits &= g.rows == 1;
+                for (const Region& g : t.dsts)
+                    fits &= (g.offset * S) % 16 == (t.dsts[0].offset * S) % 16;
                 fits &= t.dsts.size() <= (size_t)kMaxRanks && t.srcs.size() <= (size_t)kMaxRanks;
                 if (!fits || t.count == 0)
                     continue;
@@ -839,6 +854,9 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                 const uint64_t share = std::max<uint64_t>(1, (uint64_t)kInlineMaxItems * (t.count * S * nref) / moved);
                 uint64_t target = (t.count + share - 1) / share;
                 target = (target + grain - 1) / grain * grain;
+                if (!regions_aligned)
+                    target = std::min<uint64_t>(target, (op != PL_COPY && t.srcs.size() > 1 ? kInlineMisalignedReduceVectors
+                                                                                            : kInlineMisalignedCopyVectors) * E);
                 fits &= target * t.dsts.size() <= (1ull << 31);  // the kernel's 32-bit (vector, destination) index
                 inline_target[i] = target;
                 const uint64_t n = (t.count + target - 1) / target;
@@ -1265,6 +1283,12 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
 
     if (hp.inline_form && (hp.items.size() > (size_t)kInlineMaxItems || hp.refs.size() > (size_t)kInlineMaxPtrs))
         hp.inline_form = false;  // (cannot happen: the cuts above are the items)
+    // Items within those vector counts run inline over buffers at any
+    // alignment (a destination head of up to E - 1 elements goes first).
+    hp.inline_any_alignment = hp.inline_form;
+    for (const Item& it : hp.items)
+        hp.inline_any_alignment &=
+            it.cols <= (it.op ? kInlineMisalignedReduceVectors : kInlineMisalignedCopyVectors) * E + E - 1;
     pl_plan_stats& s = hp.stats;
     s.items = hp.items.size();
     s.refs = hp.refs.size();
@@ -1759,12 +1783,14 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         return st;
     if (dp->hp.inline_form) {
         // The whole plan in the launch's parameters, each reference resolved
-        // to its pointer; buffers that are not 16-byte aligned take the
-        // persistent kernel below (same items).
+        // to its pointer.  Plans with items larger than a vector per thread
+        // need 16-byte aligned buffers; small items take any alignment as long
+        // as each item's destinations share their address mod 16.  Otherwise
+        // the persistent kernel below runs the same items.
         bool aligned = true;
         for (int r = 0; r < R; ++r)
             aligned &= ((reinterpret_cast<uintptr_t>(in_bufs[r]) | reinterpret_cast<uintptr_t>(out_bufs[r])) & 15u) == 0;
-        if (aligned) {
+        if (aligned || dp->hp.inline_any_alignment) {
             const int nitems = (int)dp->hp.items.size();
             const bool small = nitems <= kInlineSmallItems && dp->hp.refs.size() <= (size_t)kInlineSmallPtrs;
             InlineSmall* is = small ? &ctx->inline_small : nullptr;
@@ -1785,11 +1811,34 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
                 char* base = f.buf < (uint32_t)R ? (char*)in_bufs[f.buf] : (char*)out_bufs[f.buf - R];
                 ptrs[k] = base + f.offset * S;
             }
-            cudaError_t e = launch_inline(dt, (dp->hp.ops & kOpsMax) != 0, is, il, nitems, (cudaStream_t)stream);
-            if (e != cudaSuccess)
-                return cuda_fail(ctx, e);
-            ++ctx->launches;
-            return PL_OK;
+            // Per item: every pointer 16-byte aligned (the kernel's shortest
+            // path), else the destinations must share their address mod 16.
+            bool congruent = true;
+            const bool all_aligned = aligned && dp->hp.all_aligned;  // aligned buffers, aligned offsets
+            for (int i = 0; congruent && i < nitems; ++i) {
+                InlineItem& it = its[i];
+                if (all_aligned) {
+                    it.flags |= kInlineAligned;
+                    continue;
+                }
+                uintptr_t any = 0;
+                for (uint32_t k = 0; k < (uint32_t)it.nsrc + it.ndst; ++k)
+                    any |= reinterpret_cast<uintptr_t>(ptrs[it.ref + k]);
+                if ((any & 15u) == 0) {
+                    it.flags |= kInlineAligned;
+                    continue;
+                }
+                const uintptr_t c0 = reinterpret_cast<uintptr_t>(ptrs[it.ref + it.nsrc]) & 15u;
+                for (uint32_t d = 1; d < it.ndst; ++d)
+                    congruent &= (reinterpret_cast<uintptr_t>(ptrs[it.ref + it.nsrc + d]) & 15u) == c0;
+            }
+            if (congruent) {
+                cudaError_t e = launch_inline(dt, (dp->hp.ops & kOpsMax) != 0, is, il, nitems, (cudaStream_t)stream);
+                if (e != cudaSuccess)
+                    return cuda_fail(ctx, e);
+                ++ctx->launches;
+                return PL_OK;
+            }
         }
     }
     LaunchArgs a{};

@@ -145,11 +145,13 @@ struct InlineItem {
     uint16_t ndst;
     uint32_t ref;
     uint32_t count;
-    uint32_t flags;  // kInlineVectorWhole
+    uint32_t flags;  // kInlineVectorWhole | kInlineAligned
 };
 // The item's destinations include one of its sources (a reduction in place):
 // one thread reads each vector and writes it to every destination.
 constexpr uint32_t kInlineVectorWhole = 1;
+// Every pointer of the item is 16-byte aligned.
+constexpr uint32_t kInlineAligned = 2;
 static_assert(sizeof(InlineItem) == 16, "InlineItem is 16 bytes");
 
 template <int NI, int NP>

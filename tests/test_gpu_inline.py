@@ -205,14 +205,16 @@ def test_allreduce_in_place_small(ctx, dtype, op, datapath_policy, n):
 
 
 @pytest.mark.parametrize("shift", [1, 3, 4])
-def test_misaligned_buffers_take_the_persistent_kernel(ctx, shift):
-    """An inline-form plan over buffers that are not 16-byte aligned."""
+def test_misaligned_buffers_inline(ctx, shift):
+    """An inline-form plan of small items over buffers off 16-byte alignment
+    (every output at the same shift): destination heads peeled, sources
+    spliced, in the inline kernel."""
     R, n, dtype = 8, 8 * 64, "bf16"
     L = P.pl_layout_partitioned(R, [64] * R)
     assert datapath(L, L, "sum", dtype, R)[0] == P.PL_ATOM_INLINE
     ins = [host("normal", dtype, 51, r, n) for r in range(R)]
-    big = [to_dev(np.concatenate([np.zeros(shift, np.uint16), a]), dtype) for a in ins]
-    views = [b[shift:] for b in big]
+    big = [to_dev(np.concatenate([np.zeros(shift + r, np.uint16), a]), dtype) for r, a in enumerate(ins)]
+    views = [b[shift + r:] for r, b in enumerate(big)]
     outs = Outs([n + shift] * R, dtype)
     ovs = [v[shift:] for v in outs.views]
     s = P.stream_handle()
@@ -222,3 +224,70 @@ def test_misaligned_buffers_take_the_persistent_kernel(ctx, shift):
     want = oracle.allreduce(ins, dtype)
     for r in range(R):
         assert_equal(to_np(ovs[r], dtype), want[r], f"rank {r}")
+
+
+def test_inline_plans_that_fall_back(ctx):
+    """The same work list on the persistent kernel: (a) small items whose
+    destinations are at different addresses mod 16 (outputs at different
+    shifts), (b) an inline plan of large items over buffers off alignment."""
+    R, dtype = 8, "bf16"
+    # (a)
+    n = 8 * 64
+    L = P.pl_layout_partitioned(R, [64] * R)
+    ins = [host("normal", dtype, 52, r, n) for r in range(R)]
+    dev = [to_dev(a, dtype) for a in ins]
+    outs = Outs([n + 8] * R, dtype)
+    ovs = [v[r % 8:] [:n] for r, v in enumerate(outs.views)]
+    s = P.stream_handle()
+    P.pl_collective(ctx, L, L, "sum", dtype, R, P.ptrs(dev), [n] * R, P.ptrs(ovs), [n] * R, None, s)
+    assert P.pl_ctx_status(ctx, s) == P.PL_OK
+    outs.check_guards()
+    want = oracle.allreduce(ins, dtype)
+    for r in range(R):
+        assert_equal(to_np(ovs[r], dtype), want[r], f"(a) rank {r}")
+    # (b) AllGather at 8 MiB per rank: inline form, items of thousands of vectors
+    n = 1 << 22
+    lens = [n // R] * R
+    lin, lout = P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens)
+    assert datapath(lin, lout, "copy", dtype, R)[0] == P.PL_ATOM_INLINE
+    gins = [host("normal", dtype, 53, r, n // R) for r in range(R)]
+    got = run(ctx, lin, lout, "copy", dtype, gins, [n] * R, None)  # aligned outputs, then misaligned
+    want = oracle.allgather(gins, dtype)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"(b) rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ALL)
+@pytest.mark.parametrize("N", [(1 << 12) + 7, (1 << 16) + 3, (1 << 19) + 5])
+def test_v_forms_inline(ctx, dtype, N):
+    """AllGatherV, ReduceScatterV (sum and maximum) and AllToAllV with Zipf
+    lengths: partitions at every misalignment, in the inline form."""
+    R = 8
+    if dtype == "fp32":
+        N = N // 2 + 1  # the same bytes
+    lens = synth.zipf_lengths(N, R, 0.125, seed=54)
+    ins = [host("normal", dtype, 54, r, lens[r]) for r in range(R)]
+    lin, lout = P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens)
+    assert datapath(lin, lout, "copy", dtype, R)[0] == P.PL_ATOM_INLINE
+    got = run(ctx, lin, lout, "copy", dtype, ins, [N] * R, None)
+    want = oracle.allgather(ins, dtype)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"AGV rank {r}")
+    if dtype != "fp8":
+        rins = [host("normal", dtype, 55, r, N) for r in range(R)]
+        for op in ("sum", "max"):
+            lin, lout = P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens)
+            assert datapath(lin, lout, op, dtype, R)[0] == P.PL_ATOM_INLINE
+            got = run(ctx, lin, lout, op, dtype, rins, lens, None)
+            want = oracle.reducescatter(rins, lens, dtype, op)
+            for r in range(R):
+                assert_equal(got[r], want[r], f"RSV {op} rank {r}")
+    if N < 1 << 17:
+        m = synth.zipf_matrix(N, R, 0.125, seed=56)
+        ains = [host("normal", dtype, 56, r, sum(m[r])) for r in range(R)]
+        lin, lout = P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m)
+        assert datapath(lin, lout, "copy", dtype, R)[0] == P.PL_ATOM_INLINE
+        got = run(ctx, lin, lout, "copy", dtype, ains, [sum(m[j][r] for j in range(R)) for r in range(R)], None)
+        want = oracle.alltoall(ains, m, dtype)
+        for r in range(R):
+            assert_equal(got[r], want[r], f"A2AV rank {r}")

@@ -260,9 +260,10 @@ def test_automatic_chunking_covers_every_element(kind, scale):
     4-SM grid: about one item per CTA for small messages (scale 1: under
     256 KiB per CTA), guided sizes that shrink along the list for larger ones
     (scale 20), claimed in order once there are more items than CTAs.
-    Executed by the emulator, the result equals the oracle."""
+    Executed by the emulator, the result equals the oracle.  (The vector
+    datapath: the persistent kernel's chunk rule, not the inline form's.)"""
     R, dtype = 8, "bf16"
-    pol = P.pl_policy_default()
+    pol = P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)
     if kind == "allgatherv":
         lens = synth.zipf_lengths(60001 * scale, R, 0.125, seed=40)
         ins = [rand(dtype, 40, r, lens[r]) for r in range(R)]
@@ -372,9 +373,11 @@ def test_inline_form_for_small_aligned_plans(coll, T):
 
 def test_inline_form_not_taken():
     """Plans the inline form does not take: moving more than 320 MiB (unless
-    every transfer reduces into one destination), staged, composed, strided,
-    misaligned, a fixed grid, a forced datapath, too many references; the form
-    forced on a plan it cannot take leaves the vector datapath."""
+    every transfer reduces into one destination between aligned regions),
+    misaligned regions whose items would exceed one vector per thread,
+    destinations of one name at different offsets mod 16 bytes, staged,
+    composed, strided, a fixed grid, a forced datapath, too many references;
+    the form forced on a plan it cannot take leaves the vector datapath."""
     R, dtype, n = 8, "bf16", 1 << 12
 
     def form(lin, lout, op, pol=None, R_=R):
@@ -402,7 +405,17 @@ def test_inline_form_not_taken():
     assert form(*uly) == P.PL_ATOM_VECTOR
     assert form(*uly, P.pl_policy_default(datapath=P.PL_ATOM_INLINE)) == P.PL_ATOM_VECTOR
     lens = synth.zipf_lengths(3001, R, 0.125, seed=71)
-    assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_VECTOR
+    assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_INLINE
+    lens = synth.zipf_lengths((1 << 22) + 1, R, 0.125, seed=71)                       # 8 MiB AllGatherV
+    assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_BULK
+    lens = synth.zipf_lengths((1 << 25) + 1, R, 0.125, seed=71)                       # 64 MiB ReduceScatterV
+    assert form(P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), "sum") == P.PL_ATOM_VECTOR
+    # one name's two destinations at offsets 0 and 3 (elements): not congruent mod 16 bytes
+    lin2 = P.pl_layout_create(2, [[(0, 0, 64)], [(1, 0, 64)]])
+    lout2 = P.pl_layout_create(2, [[(0, 0, 64), (1, 64, 64)], [(0, 3, 64), (1, 67, 64)]])
+    assert form(lin2, lout2, "copy", None, 2) == P.PL_ATOM_VECTOR
+    lout3 = P.pl_layout_create(2, [[(0, 0, 64), (1, 64, 64)], [(0, 8, 64), (1, 72, 64)]])
+    assert form(lin2, lout3, "copy", None, 2) == P.PL_ATOM_INLINE
     L64 = P.pl_layout_partitioned(64, [64] * 64)
     assert form(L64, L64, "sum", None, 64) == P.PL_ATOM_VECTOR                     # 64 x 128 references
 
