@@ -55,11 +55,13 @@ constexpr uint64_t kBulkChunkMax = 256 << 10;
 // bulk ring and pipelined items are faster).
 constexpr uint64_t kInlineAutoMoved = 320ull << 20;
 // Inline items over regions not all 16-byte aligned: at most this many body
-// vectors, which the kernel's realigning loop moves: four per thread for a
-// copy, two for a reduction (its loop holds one vector of 8 sources at a
-// time; with four a ReduceScatterV of 4 MiB per rank ran 12.0 us against the
-// persistent kernel's 10.5).
-constexpr uint64_t kInlineMisalignedCopyVectors = 4 * kInlineThreads;
+// vectors, which the kernel's realigning loop moves: eight per thread for a
+// copy (with four, an AllToAllV of 1 MiB per rank needed more than 152 items
+// and ran 8.6 us on the persistent kernel; 4.9 us inline), two for a
+// reduction (its loop holds one vector of 8 sources at a time; with four a
+// ReduceScatterV of 4 MiB per rank ran 12.0 us against the persistent
+// kernel's 10.5).
+constexpr uint64_t kInlineMisalignedCopyVectors = 8 * kInlineThreads;
 constexpr uint64_t kInlineMisalignedReduceVectors = 2 * kInlineThreads;
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {

@@ -407,6 +407,8 @@ def test_inline_form_not_taken():
     lens = synth.zipf_lengths(3001, R, 0.125, seed=71)
     assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_INLINE
     lens = synth.zipf_lengths((1 << 22) + 1, R, 0.125, seed=71)                       # 8 MiB AllGatherV
+    assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_INLINE
+    lens = synth.zipf_lengths((1 << 23) + 1, R, 0.125, seed=71)                       # 16 MiB AllGatherV
     assert form(P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy") == P.PL_ATOM_BULK
     lens = synth.zipf_lengths((1 << 25) + 1, R, 0.125, seed=71)                       # 64 MiB ReduceScatterV
     assert form(P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), "sum") == P.PL_ATOM_VECTOR
