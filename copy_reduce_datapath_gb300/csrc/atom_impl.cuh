@@ -116,21 +116,22 @@ __device__ bool wait_at_least(const unsigned long long* flag, unsigned long long
     return false;
 }
 
-__device__ __forceinline__ unsigned long long tag(const LaunchArgs& a, unsigned int use)
+// The tag of use `use` of a flag in the launch of epoch `epoch`.
+__device__ __forceinline__ unsigned long long tag(unsigned long long epoch, unsigned int use)
 {
-    return (a.epoch << 24) | (unsigned long long)(use + 1u);
+    return (epoch << 24) | (unsigned long long)(use + 1u);
 }
 
 // Warp 0 of the CTA: every wait of the item, one flag per lane (lanes take
 // flags lane, lane + 32, ...), so an item's waits overlap instead of costing
 // one round trip each.  Returns, in every lane, whether all waits passed.
-__device__ bool run_waits(const LaunchArgs& a, const Item& it, int lane)
+__device__ bool run_waits(const LaunchArgs& a, const Item& it, int lane, unsigned long long epoch)
 {
     bool ok = ld_relaxed_s32(a.st.abort) == 0;
     for (unsigned k = (unsigned)lane; ok && k < it.nwait; k += 32) {
         const Sync s = a.syncs[it.sync + k];
         const unsigned long long* f = s.type == kWaitFull ? a.st.full + s.flag : a.st.done + s.flag;
-        ok = wait_at_least(f, tag(a, s.use), a);
+        ok = wait_at_least(f, tag(epoch, s.use), a);
     }
     return __all_sync(0xffffffffu, ok) != 0;
 }
@@ -140,19 +141,19 @@ __device__ bool run_waits(const LaunchArgs& a, const Item& it, int lane)
 // ordered before each posting lane's release by the barrier, and a release
 // (st.release / atom.acq_rel at gpu scope) is cumulative, so a consumer whose
 // acquire reads the tag sees them: no separate fence is needed.
-__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index, int lane)
+__device__ void run_posts(const LaunchArgs& a, const Item& it, unsigned index, int lane, unsigned long long epoch)
 {
     for (unsigned k = (unsigned)lane; k < it.npost; k += 32) {
         const Sync s = a.syncs[it.sync + it.nwait + k];
         if (s.type == kNotify) {
             if ((long long)index == a.drop_notify)
                 continue;  // test hook: consumers of this item will time out
-            st_release(a.st.full + s.flag, tag(a, s.use));
+            st_release(a.st.full + s.flag, tag(epoch, s.use));
         } else if (s.type == kCredit) {
             unsigned old = atom_add_acq_rel(a.st.count + s.flag, 1u);
             if (old + 1u == s.count) {
                 st_relaxed_u32(a.st.count + s.flag, 0u);
-                st_release(a.st.done + s.flag, tag(a, s.use));
+                st_release(a.st.done + s.flag, tag(epoch, s.use));
             }
         }
     }
@@ -1032,7 +1033,7 @@ __device__ __forceinline__ bool put_ref(const LaunchArgs& a, const Item& it, con
 // region pointers in two ItemShared buffers (items k, k+1).
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared* sh, Slot* slot, Ref* sref, int* s_ok,
-                                                BulkRing& bk, int tid, bool bad)
+                                                BulkRing& bk, int tid, bool bad, unsigned long long epoch)
 {
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k % 3u), nxt = (int)((k + 1u) % 3u), nn = (int)((k + 2u) % 3u);
@@ -1068,7 +1069,7 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
         }
         cp_async_commit();
         if (tid < 32) {
-            const bool ok = slot[cur].item.nwait ? run_waits(a, slot[cur].item, tid) : true;
+            const bool ok = slot[cur].item.nwait ? run_waits(a, slot[cur].item, tid, epoch) : true;
             if (tid == 0)
                 *s_ok = ok ? 1 : 0;
         }
@@ -1090,7 +1091,7 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
         }
         if (tid < 32) {
             if (ok && slot[cur].item.npost)
-                run_posts(a, slot[cur].item, index, tid);
+                run_posts(a, slot[cur].item, index, tid, epoch);
             __syncwarp();
         }
     }
@@ -1103,7 +1104,7 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
 // (which made the aligned kernels 1-3% faster).  Two header slots.
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* sh, Slot* slot, int* s_ok,
-                                               BulkRing& bk, int tid, bool bad)
+                                               BulkRing& bk, int tid, bool bad, unsigned long long epoch)
 {
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k & 1u), nxt = cur ^ 1;
@@ -1125,7 +1126,7 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
                 h2 = a.items[i2];
         }
         if (tid < 32) {
-            const bool ok = it.nwait ? run_waits(a, it, tid) : true;
+            const bool ok = it.nwait ? run_waits(a, it, tid, epoch) : true;
             if (tid == 0)
                 *s_ok = ok ? 1 : 0;
         }
@@ -1144,7 +1145,7 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
         }
         __syncthreads();
         if (tid < 32 && ok && it.npost)
-            run_posts(a, it, index, tid);
+            run_posts(a, it, index, tid, epoch);
     }
 }
 
@@ -1161,6 +1162,7 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     __shared__ Slot slot[3];
     __shared__ __align__(16) Ref sref[ALIGN ? kMaxRefsPerItem : 1];
     __shared__ int s_ok;
+    __shared__ unsigned long long s_epoch;
     extern __shared__ __align__(128) char dyn[];
     BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u,
                 reinterpret_cast<unsigned long long*>(dyn) + kBulkMaxStages, 0u};
@@ -1180,6 +1182,9 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
                 mbar_init(&bk.sbar[i], 1u);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
+        // The epoch of this launch (ticketed lists, which are the ones with
+        // flags): the last CTA out of the previous one advanced it.
+        s_epoch = a.use_tickets ? *reinterpret_cast<volatile const unsigned long long*>(a.st.epoch) : 0ull;
         const unsigned i0 = claim(a, 0);
         const unsigned i1 = i0 < a.nitems ? claim(a, 1) : ~0u;
         // both header loads in flight before either is stored
@@ -1194,21 +1199,25 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
         slot[1].item = h1;
     }
     __syncthreads();
+    const unsigned long long epoch = s_epoch;
     bool bad = false;
     if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
         bad = put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
     // The loops' first barrier publishes sh[0] before item 0 moves.
     if constexpr (ALIGN)
-        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad);
+        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch);
     else
-        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad);
+        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch);
 
     if (a.use_tickets && tid == 0) {
         __threadfence();
         if (atomicAdd(a.st.exited, 1u) == gridDim.x - 1) {
-            // Last CTA out: every other CTA has taken its final ticket.
+            // Last CTA out: every other CTA has taken its final ticket and read
+            // this launch's epoch (at its start); the next launch's tags are
+            // larger than every tag of this one.
             *a.st.ticket = 0u;
             *a.st.exited = 0u;
+            *a.st.epoch = epoch + 1ull;
             __threadfence();
         }
     }

@@ -136,7 +136,6 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
     a.ops = wl.ops;
     a.all_aligned = wl.all_aligned;
     a.refs_per_item = wl.refs_per_item;
-    a.epoch = 1;  // the flags were zeroed above, so every call can use the same tags
     a.timeout_ns = 2000000000ull;
     a.drop_notify = -1;
     char* state = d->base;
@@ -148,6 +147,7 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
     a.st.exited = reinterpret_cast<unsigned int*>(tail + 4);
     a.st.status = reinterpret_cast<int*>(tail + 8);
     a.st.abort = reinterpret_cast<int*>(tail + 12);
+    a.st.epoch = reinterpret_cast<unsigned long long*>(tail + 16);  // zeroed above with the flags
     for (int r = 0; r < R; ++r) {
         a.bufs[r] = static_cast<char*>(in_bufs[r]);
         a.bufs[R + r] = static_cast<char*>(out_bufs[r]);

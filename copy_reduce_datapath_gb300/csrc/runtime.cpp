@@ -1471,7 +1471,6 @@ struct pl_ctx {
     uint32_t flag_capacity = 0;
     char* scratch = nullptr;
     uint64_t scratch_bytes = 0;
-    unsigned long long epoch = 0;
     uint64_t launches = 0;
     int last_cuda_error = 0;
     std::unordered_map<std::string, std::unique_ptr<DevicePlan>> cache;
@@ -1525,6 +1524,7 @@ pl_status ensure_flags(pl_ctx* ctx, uint32_t n)
     ctx->st.exited = (unsigned int*)(tail + 4);
     ctx->st.status = (int*)(tail + 8);
     ctx->st.abort = (int*)(tail + 12);
+    ctx->st.epoch = (unsigned long long*)(tail + 16);
     return PL_OK;
 }
 
@@ -1855,7 +1855,6 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.all_aligned = dp->hp.all_aligned;
     a.refs_per_item = dp->hp.refs_per_item;
     a.no_spread = in_place && (dp->hp.ops & kOpsReduce) ? 1 : 0;
-    a.epoch = ++ctx->epoch;
     a.timeout_ns = rp.timeout_ns;
     a.drop_notify = rp.drop_notify;
     a.st = ctx->st;

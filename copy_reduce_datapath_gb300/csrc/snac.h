@@ -88,6 +88,9 @@ struct DeviceState {
     unsigned int* exited;       // CTAs that finished (the last one resets ticket/exited)
     int* status;                // 0 ok, else a pl_status
     int* abort;                 // set with status: every wait gives up at once
+    unsigned long long* epoch;  // ticketed launches that ended; the tags of the next are
+                                // (epoch << 24) | (use + 1), so they grow from launch to launch
+                                // even when a captured CUDA graph repeats a launch's parameters
 };
 
 struct LaunchArgs {
@@ -102,7 +105,6 @@ struct LaunchArgs {
     int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
     int32_t refs_per_item;       // n > 0: item i's references are refs[i * n .. i * n + n); 0: read the header
     int32_t no_spread;           // 1: every vector is read and written by one thread (a reduction in place)
-    unsigned long long epoch;    // tags of this launch are (epoch << 24) | (use + 1)
     unsigned long long timeout_ns;
     long long drop_notify;       // item index whose notifies are skipped, or -1
     DeviceState st;

@@ -33,7 +33,10 @@
  *     GPU would share its flag words and race.
  *   - The first call for a new (layout pair, op, dtype, policy) derives a work
  *     list and uploads it with a synchronous copy; later calls reuse it.  Make
- *     that first call before capturing a stream into a CUDA graph.
+ *     that first call before capturing a stream into a CUDA graph.  A captured
+ *     call may be replayed any number of times: the SNAC flag tags of each
+ *     launch come from a device counter that every launch with flags advances,
+ *     not from the captured parameters.
  */
 #ifndef PURLIN_H
 #define PURLIN_H
