@@ -7,7 +7,8 @@ Reported value: algorithm bandwidth of the step, (T_AG + T_AR) / step time, in
 GB/s (1 GB = 1e9 bytes), summed over replicas when run on N GPUs.
 
 Also reported on the same line:
-  - sweep: latency (us) and algbw (GB/s) of AllGather and AllReduce for T = 1 KiB .. 1 GiB
+  - sweep: latency (us) and algbw (GB/s) of every collective (AllGather, AllReduce, ReduceScatter,
+    AllToAll and the three V forms) for T = 1 KiB .. 1 GiB
   - roofline: the dominant kernel (the AllReduce launch) against the measured HBM copy peak
   - e2e: the same step through the C ABI with host buffers (pinned), copies inside the timing
   - cpu_baseline: the CPU oracle on a bounded sample of the same workload
@@ -221,6 +222,59 @@ class Workload:
             self._lay[n] = (self.P.pl_layout_rank_owned(R, [n] * R), self.P.pl_layout_partitioned(R, [n] * R))
         return self._lay[n]
 
+    # The other collectives of the sweep, at T bytes per rank (the conventions
+    # of their algbw: ReduceScatter(V) and AllToAll(V) input bytes per rank,
+    # AllGatherV output bytes per rank), over the AllReduce's buffers (and, for
+    # the AllToAllV's column sums, buffers of their own).  V forms: Zipf
+    # s = 0.125 lengths, seed 4.
+    _sweep = {}
+
+    def _sweep_layouts(self, name, T):
+        import synth
+        P = self.P
+        key = (name, T)
+        if key not in self._sweep:
+            N = T // 2
+            if name == "reducescatter":
+                lens = [N // R] * R
+                self._sweep[key] = (P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), lens)
+            elif name == "alltoall":
+                m = [[N // R] * R for _ in range(R)]
+                self._sweep[key] = (P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), m)
+            elif name in ("allgatherv", "reducescatterv"):
+                lens = synth.zipf_lengths(N, R, 0.125, seed=4)
+                lo, lp = P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens)
+                self._sweep[key] = (lo, lp, lens) if name == "allgatherv" else (lp, lo, lens)
+            else:
+                m = synth.zipf_matrix(N, R, 0.125, seed=4)
+                self._sweep[key] = (P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), m)
+        return self._sweep[key]
+
+    def sweep_call(self, name, T, ctx, stream):
+        """A closure that launches collective `name` at T bytes per rank on `stream`."""
+        import torch
+        P = self.P
+        N = T // 2
+        lin, lout, shape = self._sweep_layouts(name, T)
+        if name in ("reducescatter", "reducescatterv"):
+            ins, outs = self.ar_in, [o[: shape[r]] for r, o in enumerate(self.ar_out)]
+            cin, cout, op = [N] * R, list(shape), "sum"
+        elif name == "allgatherv":
+            ins, outs = [x[: shape[r]] for r, x in enumerate(self.ar_in)], self.ag_out
+            cin, cout, op = list(shape), [N] * R, "copy"
+        else:
+            cols = [sum(shape[j][r] for j in range(R)) for r in range(R)]
+            if name == "alltoall":
+                outs = self.ar_out
+            else:
+                if not hasattr(self, "a2av_out") or self.a2av_out[0].numel() < max(cols):
+                    self.a2av_out = [torch.empty(max(cols), dtype=torch.bfloat16, device=self.ar_in[0].device)
+                                     for _ in range(R)]
+                outs = self.a2av_out
+            ins, cin, cout, op = self.ar_in, [N] * R, cols, "copy"
+        pi, po = P.ptrs(ins), P.ptrs(outs)
+        return lambda: P.pl_collective(ctx, lin, lout, op, "bf16", R, pi, cin, po, cout, None, stream)
+
 
 def sampled_parity(wl, device):
     """Windows of the full-size outputs against the oracle on the same input windows."""
@@ -248,10 +302,14 @@ def sampled_parity(wl, device):
     return bad == 0
 
 
+SWEEP_OTHERS = ("reducescatter", "alltoall", "allgatherv", "reducescatterv", "alltoallv")
+
+
 def time_sweep(ctx, wl, stream, torch):
-    """Latency and algbw per size.  Up to 64 MiB each point is a CUDA graph of
-    `calls` launches replayed on the launch stream (device time per call, no
-    host launch overhead); above that, events around back-to-back calls."""
+    """Latency and algbw per size and collective (R = 8, bf16; V forms with
+    Zipf lengths).  Up to 64 MiB each point is a CUDA graph of `calls`
+    launches replayed on the launch stream (device time per call, no host
+    launch overhead); above that, events around back-to-back calls."""
     out = []
     for e in range(10, 31):
         T = 1 << e
@@ -262,6 +320,9 @@ def time_sweep(ctx, wl, stream, torch):
             n = T // 2 // R if name == "allgather" else T // 2
             fn = getattr(wl, name)
             us, how = time_call(lambda: fn(ctx, stream.cuda_stream, n), T, stream, torch)
+            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
+        for name in SWEEP_OTHERS:
+            us, how = time_call(wl.sweep_call(name, T, ctx, stream.cuda_stream), T, stream, torch)
             row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
         out.append(row)
     return out

@@ -850,15 +850,28 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
     // Scalar head and tail elements (and, see above, misaligned rows of aligned kernels).
     for (unsigned e = tid; e < head + ntail; e += nthr) {
         const unsigned i = e < head ? e : tail0 + (e - head);
-        uint32_t v = EL::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
+        uint32_t v;
         if constexpr (REDUCE) {
             if (nsrc > 1) {
-                float acc = EL::to_f(v);
+                // 8 source loads issued before any is folded, in rank order
+                float acc = 0.f;
 #pragma unroll 1
-                for (int s = 1; s < nsrc; ++s)
-                    acc = combine<MAXOP>(acc, EL::to_f(EL::load(SRC_ROW(sh, s, row) + (size_t)i * S)));
+                for (int s0 = 0; s0 < nsrc; s0 += 8) {
+                    uint32_t y[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        y[q] = s0 + q < nsrc ? EL::load(SRC_ROW(sh, s0 + q, row) + (size_t)i * S) : 0u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (s0 + q < nsrc)
+                            acc = s0 + q == 0 ? EL::to_f(y[q]) : combine<MAXOP>(acc, EL::to_f(y[q]));
+                }
                 v = EL::from_f(acc);
+            } else {
+                v = EL::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
             }
+        } else {
+            v = EL::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
         }
 #pragma unroll 1
         for (unsigned long long m = mask; m; m &= m - 1) {
@@ -1284,6 +1297,27 @@ cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_
 
 // ------------------------------------------------- inline-parameter kernel
 
+// The rank-ordered reduction (fp32 sum or maximum, rounded once) of the
+// element at byte offset `off` of the ns sources p[0 ..]: 8 loads issued
+// before any is folded.
+template <int DT, bool MAXOP>
+__device__ __forceinline__ uint32_t scalar_reduce(char* const* p, unsigned ns, size_t off)
+{
+    using EL = Elem<DT>;
+    float acc = 0.f;
+    for (unsigned s0 = 0; s0 < ns; s0 += 8) {
+        uint32_t y[8];
+#pragma unroll
+        for (unsigned q = 0; q < 8; ++q)
+            y[q] = s0 + q < ns ? EL::load(p[s0 + q] + off) : 0u;
+#pragma unroll
+        for (unsigned q = 0; q < 8; ++q)
+            if (s0 + q < ns)
+                acc = s0 + q == 0 ? EL::to_f(y[q]) : combine<MAXOP>(acc, EL::to_f(y[q]));
+    }
+    return EL::from_f(acc);
+}
+
 // The rank-ordered reduction (fp32 sum or maximum, rounded once) of the 16
 // bytes at byte offset `off` of the ns sources p[0 ..], 8 sources in flight.
 // ALIGNED: every source address is 16-byte aligned.  Otherwise a source at a
@@ -1353,6 +1387,7 @@ __global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __
     const bool whole = (it.flags & kInlineVectorWhole) != 0;
     const bool reduce = EL::kReducible && ns > 1;
     unsigned h = 0, nv = n / E;
+    unsigned busy = step;  // threads the body's first round keeps busy
     if (it.flags & kInlineAligned) {
         if (nv > step) {
             if (!reduce) {
@@ -1409,6 +1444,7 @@ __global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __
             }
         } else if (nv > 0) {
             const unsigned g = whole ? 1u : max(1u, min(nd, step / nv));
+            busy = nv * g;
             if (tid < nv * g) {
                 const unsigned j = tid / nv, v = tid - j * nv;
                 const size_t off = (size_t)v * 16;
@@ -1431,6 +1467,7 @@ __global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __
         const size_t body = (size_t)h * S;
         const unsigned g = whole || nv > step ? 1u : max(1u, min(nd, step / max(nv, 1u)));
         const unsigned total = nv * g;
+        busy = min(step, total);
         if (!reduce) {
             // one source at shift q: its aligned vectors, loaded before any splice
             constexpr int U = 4;
@@ -1466,30 +1503,19 @@ __global__ void __launch_bounds__(kInlineThreads, 1) snac_inline_kernel(const __
             }
         }
     }
-    // head [0, h) and tail [h + nv * E, n), one element each
+    // head [0, h) and tail [h + nv * E, n), one element each, first on the
+    // threads the body left idle (so both are in flight at once)
     const unsigned t0 = h + nv * E, ne = h + (n - t0);
     if (ne == 0)
         return;
     const unsigned gt = whole ? 1u : max(1u, min(nd, step / ne));
-    for (unsigned k = tid; k < ne * gt; k += step) {
+    for (unsigned k = (tid + step - busy % step) % step; k < ne * gt; k += step) {
         const unsigned i = k % ne, e = i < h ? i : t0 + (i - h);
-        uint32_t x = EL::load(p[0] + (size_t)e * S);
+        uint32_t x;
         if constexpr (EL::kReducible) {
-            if (ns > 1) {
-                // sources 8 at a time in flight, folded in rank order
-                float acc = EL::to_f(x);
-                for (unsigned s0 = 1; s0 < ns; s0 += 8) {
-                    uint32_t y[8];
-#pragma unroll
-                    for (unsigned q = 0; q < 8; ++q)
-                        y[q] = s0 + q < ns ? EL::load(p[s0 + q] + (size_t)e * S) : 0u;
-#pragma unroll
-                    for (unsigned q = 0; q < 8; ++q)
-                        if (s0 + q < ns)
-                            acc = combine<MAXOP>(acc, EL::to_f(y[q]));
-                }
-                x = EL::from_f(acc);
-            }
+            x = reduce ? scalar_reduce<DT, MAXOP>(p, ns, (size_t)e * S) : EL::load(p[0] + (size_t)e * S);
+        } else {
+            x = EL::load(p[0] + (size_t)e * S);
         }
         for (unsigned d = k / ne; d < nd; d += gt)
             EL::store(p[ns + d] + (size_t)e * S, x);

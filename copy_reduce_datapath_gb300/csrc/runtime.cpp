@@ -63,6 +63,14 @@ constexpr uint64_t kInlineAutoMoved = 320ull << 20;
 // kernel's 10.5).
 constexpr uint64_t kInlineMisalignedCopyVectors = 8 * kInlineThreads;
 constexpr uint64_t kInlineMisalignedReduceVectors = 2 * kInlineThreads;
+// A copy into one destination stores a vector once: twice the vectors.
+constexpr uint64_t kInlineMisalignedOneDstVectors = 16 * kInlineThreads;
+
+uint64_t misaligned_cap(bool reduction, size_t ndst)
+{
+    return reduction ? kInlineMisalignedReduceVectors : ndst == 1 ? kInlineMisalignedOneDstVectors
+                                                                  : kInlineMisalignedCopyVectors;
+}
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
@@ -857,8 +865,8 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                 uint64_t target = (t.count + share - 1) / share;
                 target = (target + grain - 1) / grain * grain;
                 if (!regions_aligned)
-                    target = std::min<uint64_t>(target, (op != PL_COPY && t.srcs.size() > 1 ? kInlineMisalignedReduceVectors
-                                                                                            : kInlineMisalignedCopyVectors) * E);
+                    target = std::min<uint64_t>(target, misaligned_cap(op != PL_COPY && t.srcs.size() > 1,
+                                                                       t.dsts.size()) * E);
                 fits &= target * t.dsts.size() <= (1ull << 31);  // the kernel's 32-bit (vector, destination) index
                 inline_target[i] = target;
                 const uint64_t n = (t.count + target - 1) / target;
@@ -1289,8 +1297,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     // alignment (a destination head of up to E - 1 elements goes first).
     hp.inline_any_alignment = hp.inline_form;
     for (const Item& it : hp.items)
-        hp.inline_any_alignment &=
-            it.cols <= (it.op ? kInlineMisalignedReduceVectors : kInlineMisalignedCopyVectors) * E + E - 1;
+        hp.inline_any_alignment &= it.cols <= misaligned_cap(it.op != 0, it.ndst) * E + E - 1;
     pl_plan_stats& s = hp.stats;
     s.items = hp.items.size();
     s.refs = hp.refs.size();
