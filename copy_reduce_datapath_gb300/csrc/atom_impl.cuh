@@ -390,19 +390,26 @@ template <int DT, bool MAXOP> struct Acc {
 };
 
 // The 16 bytes that start q bytes into the 32-byte pair (lo, hi), 0 <= q < 16.
+// q is the same for every vector of a row (a warp-uniform branch): the word
+// offset q / 4 picks the words, and four funnel shifts by (q mod 4) bytes
+// join them.
 __device__ __forceinline__ uint4 realign(uint4 lo, uint4 hi, int q)
 {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    const int k = q >> 2;
     const unsigned sh = (unsigned)(q & 3) * 8u;
-    uint32_t r[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const uint32_t a0 = k == 0 ? w[m] : k == 1 ? w[m + 1] : k == 2 ? w[m + 2] : w[m + 3];
-        const uint32_t a1 = k == 0 ? w[m + 1] : k == 1 ? w[m + 2] : k == 2 ? w[m + 3] : w[m + 4];
-        r[m] = __funnelshift_r(a0, a1, sh);
+    switch (q >> 2) {
+    case 0:
+        return make_uint4(__funnelshift_r(lo.x, lo.y, sh), __funnelshift_r(lo.y, lo.z, sh),
+                          __funnelshift_r(lo.z, lo.w, sh), __funnelshift_r(lo.w, hi.x, sh));
+    case 1:
+        return make_uint4(__funnelshift_r(lo.y, lo.z, sh), __funnelshift_r(lo.z, lo.w, sh),
+                          __funnelshift_r(lo.w, hi.x, sh), __funnelshift_r(hi.x, hi.y, sh));
+    case 2:
+        return make_uint4(__funnelshift_r(lo.z, lo.w, sh), __funnelshift_r(lo.w, hi.x, sh),
+                          __funnelshift_r(hi.x, hi.y, sh), __funnelshift_r(hi.y, hi.z, sh));
+    default:
+        return make_uint4(__funnelshift_r(lo.w, hi.x, sh), __funnelshift_r(hi.x, hi.y, sh),
+                          __funnelshift_r(hi.y, hi.z, sh), __funnelshift_r(hi.z, hi.w, sh));
     }
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // ------------------------------------------------------------ the datapath
@@ -696,6 +703,11 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
     const unsigned per = q ? 31u : 32u;  // outputs per warp step
     const unsigned span = per * ((unsigned)nthr >> 5);
     const unsigned lim = q ? nv + 1u : nv;
+    // A copy into one destination (the AllToAll(V) shape): its row pointer
+    // once, not per vector.  (Not for reductions: the extra registers cost
+    // their kernels more than the loads saved.)
+    const bool one = !SUM && (mask & (mask - 1)) == 0;
+    char* const d1 = SUM ? nullptr : DST_ROW(sh, __ffsll((long long)mask) - 1, row) + body;
     for (unsigned g0 = warp * per; g0 < nv; g0 += span * U) {
         uint4 r[U];
         if constexpr (!SUM) {
@@ -748,10 +760,14 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
             }
             const unsigned out = g0 + u * span + lane;
             if ((unsigned)lane < per && out < nv) {
+                if (!SUM && one) {
+                    st16(d1 + (size_t)out * 16, v);
+                } else {
 #pragma unroll 1
-                for (unsigned long long m = mask; m; m &= m - 1) {
-                    const int d = __ffsll((long long)m) - 1;
-                    st16(DST_ROW(sh, d, row) + body + (size_t)out * 16, v);
+                    for (unsigned long long m = mask; m; m &= m - 1) {
+                        const int d = __ffsll((long long)m) - 1;
+                        st16(DST_ROW(sh, d, row) + body + (size_t)out * 16, v);
+                    }
                 }
             }
         }
