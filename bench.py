@@ -275,6 +275,31 @@ class Workload:
         pi, po = P.ptrs(ins), P.ptrs(outs)
         return lambda: P.pl_collective(ctx, lin, lout, op, "bf16", R, pi, cin, po, cout, None, stream)
 
+    def sweep_form(self, name, T, num_sms):
+        """The launch form the automatic policy takes for collective `name` at T
+        bytes per rank (host-side plan derivation; 16-byte aligned buffers)."""
+        import synth
+        P = self.P
+        if name == "allgather":
+            lin, lout = self._layouts(T // 2 // R)
+            op = "copy"
+        elif name == "allreduce":
+            key = ("allreduce", T)
+            if key not in self._sweep:
+                L = P.pl_layout_partitioned(R, synth.equal_lengths(T // 2, R))
+                self._sweep[key] = (L, L, None)
+            lin, lout, _ = self._sweep[key]
+            op = "sum"
+        else:
+            lin, lout, _ = self._sweep_layouts(name, T)
+            op = "sum" if name in ("reducescatter", "reducescatterv") else "copy"
+        plan = P.pl_plan_create(lin, lout, op, "bf16", R, None, num_sms)
+        try:
+            st = P.pl_plan_get_stats(plan)
+        finally:
+            P.pl_plan_destroy(plan)
+        return {P.PL_ATOM_INLINE: "inline", P.PL_ATOM_BULK: "bulk", P.PL_ATOM_VECTOR: "vector"}.get(st.datapath, "?")
+
 
 def sampled_parity(wl, device):
     """Windows of the full-size outputs against the oracle on the same input windows."""
@@ -311,6 +336,7 @@ def time_sweep(ctx, wl, stream, torch):
     launches replayed on the launch stream (device time per call, no host
     launch overhead); above that, events around back-to-back calls."""
     out = []
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     for e in range(10, 31):
         T = 1 << e
         if T > wl.T:
@@ -320,10 +346,12 @@ def time_sweep(ctx, wl, stream, torch):
             n = T // 2 // R if name == "allgather" else T // 2
             fn = getattr(wl, name)
             us, how = time_call(lambda: fn(ctx, stream.cuda_stream, n), T, stream, torch)
-            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
+            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how,
+                         "form": wl.sweep_form(name, T, sms)}
         for name in SWEEP_OTHERS:
             us, how = time_call(wl.sweep_call(name, T, ctx, stream.cuda_stream), T, stream, torch)
-            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how}
+            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how,
+                         "form": wl.sweep_form(name, T, sms)}
         out.append(row)
     return out
 
