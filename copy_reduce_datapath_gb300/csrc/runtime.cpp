@@ -1484,7 +1484,7 @@ struct pl_ctx {
     std::map<std::pair<int, uint64_t>, pl_layout*> ar_layouts;
     // Host images of the inline kernel's parameter blocks (copied by each launch).
     InlineSmall inline_small{};
-    std::unique_ptr<InlineLarge> inline_large = std::make_unique<InlineLarge>();
+    std::unique_ptr<InlineLarge> inline_large;
 };
 
 namespace {
@@ -1687,6 +1687,9 @@ PL_API pl_status pl_ctx_create(pl_ctx** out, int device, uint64_t scratch_bytes)
     std::unique_ptr<pl_ctx> ctx(new (std::nothrow) pl_ctx);
     if (!ctx)
         return PL_ERR_NOMEM;
+    ctx->inline_large.reset(new (std::nothrow) InlineLarge);
+    if (!ctx->inline_large)
+        return PL_ERR_NOMEM;
     ctx->device = device;
     DeviceGuard g(device);
     if (!g.ok())
@@ -1815,16 +1818,19 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
                 const bool whole = in_place && it.nsrc > 1 && it.ndst > 1;
                 its[i] = InlineItem{it.nsrc, it.ndst, it.ref, (uint32_t)it.cols, whole ? kInlineVectorWhole : 0u};
             }
-            for (size_t k = 0; k < dp->hp.refs.size(); ++k) {
+            // Zero-staging items reference inputs and outputs only; anything
+            // else takes the persistent kernel.
+            bool usable = true;
+            for (size_t k = 0; usable && k < dp->hp.refs.size(); ++k) {
                 const Ref& f = dp->hp.refs[k];
-                char* base = f.buf < (uint32_t)R ? (char*)in_bufs[f.buf] : (char*)out_bufs[f.buf - R];
-                ptrs[k] = base + f.offset * S;
+                usable = f.buf < 2u * (uint32_t)R;
+                if (usable)
+                    ptrs[k] = (f.buf < (uint32_t)R ? (char*)in_bufs[f.buf] : (char*)out_bufs[f.buf - R]) + f.offset * S;
             }
             // Per item: every pointer 16-byte aligned (the kernel's shortest
             // path), else the destinations must share their address mod 16.
-            bool congruent = true;
             const bool all_aligned = aligned && dp->hp.all_aligned;  // aligned buffers, aligned offsets
-            for (int i = 0; congruent && i < nitems; ++i) {
+            for (int i = 0; usable && i < nitems; ++i) {
                 InlineItem& it = its[i];
                 if (all_aligned) {
                     it.flags |= kInlineAligned;
@@ -1839,9 +1845,9 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
                 }
                 const uintptr_t c0 = reinterpret_cast<uintptr_t>(ptrs[it.ref + it.nsrc]) & 15u;
                 for (uint32_t d = 1; d < it.ndst; ++d)
-                    congruent &= (reinterpret_cast<uintptr_t>(ptrs[it.ref + it.nsrc + d]) & 15u) == c0;
+                    usable &= (reinterpret_cast<uintptr_t>(ptrs[it.ref + it.nsrc + d]) & 15u) == c0;
             }
-            if (congruent) {
+            if (usable) {
                 cudaError_t e = launch_inline(dt, (dp->hp.ops & kOpsMax) != 0, is, il, nitems, (cudaStream_t)stream);
                 if (e != cudaSuccess)
                     return cuda_fail(ctx, e);
