@@ -417,6 +417,7 @@ struct HostPlan {
     int refs_per_item = 0;  // n > 0: every item has n references, item i's at [i * n, i * n + n)
     bool inline_form = false;  // one-row items that the inline-parameter kernel runs, one per CTA
     bool inline_any_alignment = false;  // ... over buffers at any alignment (small items)
+    bool flagged_reduction = false;     // a list with flags that reduces: the two-CTA kernels
     pl_plan_stats stats{};
 };
 
@@ -750,8 +751,21 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
         for (const auto* side : {&t.srcs, &t.dsts})
             for (const Region& g : *side)
                 regions_aligned &= (g.offset * S) % 16 == 0 && (g.rows == 1 || (g.stride * S) % 16 == 0);
+    const bool staged = pol.path == PL_PATH_STAGED;
+    bool multi_dst_sum = false;
+    for (const Transfer& t : ts)
+        multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
+    const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
+    // Lists with flags that reduce (staged, composed) run the two-CTA kernels
+    // even when aligned: their waits leave the single CTA's warps idle
+    // (measured at 1 GiB: staged AllReduce 7.0 -> 5.9 ms, staged ReduceScatter
+    // 5.6 -> 4.9 ms, composed AllReduce 3.25 -> 3.18 ms; staged copies lose:
+    // AllGather 2.5 -> 2.9 ms, so they keep one CTA).
+    hp.flagged_reduction = ticketed && op != PL_COPY;
     // (The bulk ring's shared memory holds one CTA per SM, whatever the kernel.)
-    const int full_grid = std::max(1, num_sms) * std::max(1, regions_aligned || bulk ? occ.aligned : occ.spliced);
+    const int full_grid =
+        std::max(1, num_sms) *
+        std::max(1, (regions_aligned || bulk) && !hp.flagged_reduction ? occ.aligned : occ.spliced);
     uint64_t chunk_bytes = pol.chunk_bytes;
     if (chunk_bytes == 0) {
         chunk_bytes = total_bytes / ((uint64_t)full_grid * kItemsPerCta);
@@ -759,11 +773,6 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     }
     chunk_bytes = std::max<uint64_t>(256, chunk_bytes / 256 * 256);
 
-    const bool staged = pol.path == PL_PATH_STAGED;
-    bool multi_dst_sum = false;
-    for (const Transfer& t : ts)
-        multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
-    const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
     // The staged path keeps chunks small, so that a ring of a given size holds
     // many rows of them (measured: the staged AllReduce does not gain from
     // larger chunks, the staged ReduceScatter loses).  The zero-staging
@@ -1865,7 +1874,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.dtype = dt;
     a.nbufs = 2 * R + 1;
     a.ops = dp->hp.ops;
-    a.all_aligned = dp->hp.all_aligned;
+    a.all_aligned = dp->hp.all_aligned && !dp->hp.flagged_reduction;
     a.refs_per_item = dp->hp.refs_per_item;
     a.no_spread = in_place && (dp->hp.ops & kOpsReduce) ? 1 : 0;
     a.timeout_ns = rp.timeout_ns;
@@ -1882,7 +1891,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
         stages = kBulkMaxStages;
     // The bulk ring's shared memory holds one CTA per SM: a grid sized for the
     // two-CTA spliced kernels is trimmed to one CTA per SM (claims adapt).
-    const int ctas = bulk && !dp->hp.all_aligned ? std::min(ps.ctas, ctx->num_sms) : ps.ctas;
+    const int ctas = bulk && !a.all_aligned ? std::min(ps.ctas, ctx->num_sms) : ps.ctas;
     cudaError_t e = launch_snac(a, ctas, bulk, stages, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(ctx, e);
@@ -1954,7 +1963,7 @@ int derive_staged_allreduce(int R, int dtype, uint64_t count, void* const* in_bu
     out.syncs = std::move(hp.syncs);
     out.nflags = hp.nflags;
     out.ops = hp.ops;
-    out.all_aligned = hp.all_aligned;
+    out.all_aligned = hp.all_aligned && !hp.flagged_reduction;
     out.refs_per_item = hp.refs_per_item;
     out.ctas = hp.stats.ctas;
     out.uses_tickets = hp.stats.uses_tickets;
