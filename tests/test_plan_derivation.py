@@ -435,3 +435,28 @@ def test_forced_inline_cuts_at_most_152_items():
     want = oracle.allgather(ins, dtype)
     outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window=16, seed=9)
+
+
+def test_flagged_reductions_take_two_ctas_per_sm():
+    """Lists with flags that reduce (staged, composed) are sized for the two-CTA
+    kernels even when aligned; staged copies and unflagged lists keep one CTA
+    per SM when aligned."""
+    R, dtype, n = 8, "bf16", 1 << 22
+    L = P.pl_layout_partitioned(R, [n // R] * R)
+    lo = P.pl_layout_rank_owned(R, [n // R] * R)
+
+    def ctas(lin, lout, op, pol):
+        pl = P.pl_plan_create(lin, lout, op, dtype, R, pol, num_sms=152, scratch_bytes=64 << 20)
+        try:
+            return P.pl_plan_get_stats(pl).ctas
+        finally:
+            P.pl_plan_destroy(pl)
+
+    staged = P.pl_policy_default(path=P.PL_PATH_STAGED)
+    composed = P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED)
+    vector = P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)
+    assert ctas(L, L, "sum", staged) == 304
+    assert ctas(L, lo, "sum", staged) == 304
+    assert ctas(L, L, "sum", composed) == 304
+    assert ctas(lo, L, "copy", staged) == 152
+    assert ctas(L, L, "sum", vector) == 152
