@@ -1038,7 +1038,7 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
             if (!staged) {
                 if (sum && t.dsts.size() > 1 && pol.ar_form == PL_AR_COMPOSED) {
                     // Figure 6, zero-staging: the owner reduces the chunk into its
-                    // output and notifies; every other rank then copies it.
+                    // output and notifies; one item then copies it to every other rank.
                     tickets = true;
                     size_t o = owner_of(t);
                     uint32_t flag = next_flag++;
@@ -1050,17 +1050,17 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
                     put(c, 0, red, kMove, op, ch);
                     bytes_read += blk * t.srcs.size();
                     bytes_written += blk;
-                    for (size_t d = 0; d < t.dsts.size(); ++d) {
-                        if (d == o)
-                            continue;
-                        Builder::Pending ag;
-                        ag.src.push_back(b.region(t.dsts[o], ch));
-                        ag.dst.push_back(b.region(t.dsts[d], ch));
-                        ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
-                        put(c, 2, ag, kConsume, PL_COPY, ch);
-                        bytes_read += blk;
-                        bytes_written += blk;
-                    }
+                    // The gather: one item reads the owner's chunk once and
+                    // writes it to every other rank (an AllGather item).
+                    Builder::Pending ag;
+                    ag.src.push_back(b.region(t.dsts[o], ch));
+                    for (size_t d = 0; d < t.dsts.size(); ++d)
+                        if (d != o)
+                            ag.dst.push_back(b.region(t.dsts[d], ch));
+                    ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
+                    put(c, 2, ag, kConsume, PL_COPY, ch);
+                    bytes_read += blk;
+                    bytes_written += blk * (t.dsts.size() - 1);
                 } else {
                     // Zero-staging Consume: read the sources, write every destination.
                     for (size_t d0 = 0; d0 < t.dsts.size(); d0 += kMaxRanks) {
