@@ -197,6 +197,8 @@ class Workload:
         lens = [self.n_ag] * R
         self.ag_lin = P.pl_layout_rank_owned(R, lens)
         self.ag_lout = P.pl_layout_partitioned(R, lens)
+        self._lay = {}    # AllGather layouts per element count
+        self._sweep = {}  # the other collectives' layouts per (name, T)
 
     def allgather(self, ctx, stream, n=None, ins=None, outs=None):
         P = self.P
@@ -215,8 +217,6 @@ class Workload:
         P.pl_allreduce(ctx, "bf16", R, self.n_ar if n is None else n, P.ptrs(ins or self.ar_in),
                        P.ptrs(outs or self.ar_out), None, stream)
 
-    _lay = {}
-
     def _layouts(self, n):
         if n not in self._lay:
             self._lay[n] = (self.P.pl_layout_rank_owned(R, [n] * R), self.P.pl_layout_partitioned(R, [n] * R))
@@ -227,8 +227,6 @@ class Workload:
     # AllGatherV output bytes per rank), over the AllReduce's buffers (and, for
     # the AllToAllV's column sums, buffers of their own).  V forms: Zipf
     # s = 0.125 lengths, seed 4.
-    _sweep = {}
-
     def _sweep_layouts(self, name, T):
         import synth
         P = self.P
