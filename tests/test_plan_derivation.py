@@ -460,3 +460,27 @@ def test_flagged_reductions_take_two_ctas_per_sm():
     assert ctas(L, L, "sum", composed) == 304
     assert ctas(lo, L, "copy", staged) == 152
     assert ctas(L, L, "sum", vector) == 152
+
+
+def test_composed_gather_reads_the_owners_chunk_once():
+    """Zero-staging composed AllReduce (Figure 6): per chunk, the owner's reduce
+    (R sources, one destination, then a Notify) and one gather item that waits
+    for it and copies the reduced chunk to the R - 1 other ranks.  Bytes over
+    all chunks: the reduces read R x n and write n elements, the gathers read n
+    and write (R - 1) x n.  The emulator gives the oracle's result."""
+    R, dtype, n = 8, "bf16", 8 * 3000 + 5
+    ins = [rand(dtype, 73, r, n) for r in range(R)]
+    L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
+    pl = plan_for(L, L, "sum", dtype, R, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=1024))
+    st, items = plan_interp.load_plan(pl)
+    reduces = [(it, syncs) for it, _, syncs in items if it.nsrc == R]
+    gathers = [(it, syncs) for it, _, syncs in items if it.nsrc == 1]
+    assert len(reduces) == len(gathers) > 0
+    assert all(it.ndst == 1 and it.npost == 1 for it, _ in reduces)
+    assert all(it.ndst == R - 1 and it.nwait == 1 for it, _ in gathers)
+    S = 2
+    assert st.bytes_read == R * n * S + n * S
+    assert st.bytes_written == n * S + (R - 1) * n * S
+    want = oracle.allreduce(ins, dtype)
+    outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=11)
