@@ -484,3 +484,25 @@ def test_composed_gather_reads_the_owners_chunk_once():
     want = oracle.allreduce(ins, dtype)
     outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=11)
+
+
+def test_one_to_one_plans_take_one_item_per_cta_up_to_512_kib():
+    """An AllToAllV of 16 MiB per rank (about 431 KB per CTA of a 304-CTA grid):
+    one item per CTA, no ticket; at 64 MiB per rank, guided items claimed in
+    order."""
+    R = 8
+
+    def stats(T):
+        N = T // 2
+        m = synth.zipf_matrix(N, R, 0.125, seed=4)
+        pl = P.pl_plan_create(P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), "copy", "bf16", R,
+                              P.pl_policy_default(datapath=P.PL_ATOM_VECTOR), num_sms=152)
+        try:
+            return P.pl_plan_get_stats(pl)
+        finally:
+            P.pl_plan_destroy(pl)
+
+    st = stats(16 << 20)
+    assert st.items == st.ctas and st.uses_tickets == 0
+    st = stats(64 << 20)
+    assert st.items > st.ctas and st.uses_tickets == 1
