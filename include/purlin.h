@@ -293,7 +293,7 @@ typedef struct pl_plan_stats {
     uint64_t chunk_elems;  /* elements per chunk */
     uint64_t slots;        /* scratch ring slots per rank (staged path; 0 otherwise) */
     uint64_t slot_elems;   /* elements per slot */
-    int32_t ctas;          /* persistent grid size */
+    int32_t ctas;          /* persistent grid size (the inline form: one CTA per item) */
     int32_t threads;       /* threads per CTA */
     int32_t uses_tickets;  /* 1 = items are claimed in order through a device counter */
     int32_t path;          /* resolved PL_PATH_* */
