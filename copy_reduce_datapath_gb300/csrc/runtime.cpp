@@ -683,8 +683,6 @@ bool waits_precede(const HostPlan& hp)
     return true;
 }
 
-// Derives the work list with consumers emitted `lag` chunk rows behind the
-// producers they wait for (so the CTAs that claim them in order rarely spin).
 // Codesign policy for the datapath of the persistent kernel: large copy-only
 // plans stream through the bulk-copy ring (one shared-memory read per chunk,
 // one bulk store per destination) when their regions are 16-byte aligned, or
@@ -701,568 +699,682 @@ bool launch_bulk(const HostPlan& hp, const ResolvedPolicy& pol)
            ps.bytes_read + ps.bytes_written >= kBulkAutoBytes;
 }
 
-pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
-                       const ResolvedPolicy& pol, int num_sms, Occupancy occ, uint64_t scratch_bytes, int lag,
-                       HostPlan& hp)
-{
-    if (in.R != R || out.R != R)
-        return PL_ERR_INVALID;
-    hp = HostPlan{};
-    hp.R = R;
-    hp.dtype = dt;
-    const uint64_t S = elem_size(dt);
-    const uint64_t E = 16 / S;
+// ---------------------------------------------------------------------------
+// The derivation in three parts (Figure 1 caption: codesign policies tune the
+// execution without changing the collective):
+//   analyse        the layout pair -> its transfers and the facts about them;
+//   choose_policy  those facts + the caller's policy -> chunk rule, chunk and
+//                  slot sizes, grid, staged or zero-staging;
+//   emit_items     transfers + policy -> work items, flags and ring slots in
+//                  claim order (the SNAC steps of the abstract and Figure 6).
+// ---------------------------------------------------------------------------
 
+// What a layout pair asks for, before any policy.
+struct PlanShape {
     std::vector<Transfer> ts;
-    pl_status st = collect_transfers(in, out, op, R, ts);
+    uint64_t S = 0;                   // element bytes
+    uint64_t E = 0;                   // elements per 16-byte vector
+    uint64_t total_bytes = 0;         // bytes of every transfer's region, counted once
+    uint64_t moved = 0, rd = 0, wr = 0;  // zero-staging bytes read + written, read, written
+    uint64_t fanout = 2;              // most references (sources + destinations) of one transfer
+    bool copy_like = true;            // COPY, or every transfer has one source
+    bool one_row = true;              // every region is one row
+    bool all_aligned_regions = true;  // every region offset is a multiple of 16 bytes
+    bool regions_aligned = true;      // ... and so is every multi-row region's row stride
+    bool multi_dst_sum = false;       // a reduction with several destinations (the AllReduce shape)
+    bool rs_shape = false;            // every transfer reduces several sources into one destination
+    bool equal = true;                // one-row transfers of one size and fan-out
+    bool one_to_one = true;           // every transfer has one source and one destination
+};
+
+pl_status analyse(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R, PlanShape& sh)
+{
+    sh = PlanShape{};
+    sh.S = elem_size(dt);
+    sh.E = 16 / sh.S;
+    pl_status st = collect_transfers(in, out, op, R, sh.ts);
     if (st != PL_OK)
         return st;
-    uint64_t total_bytes = 0;
-    for (Transfer& t : ts) {
+    const uint64_t S = sh.S;
+    sh.rs_shape = op != PL_COPY;
+    for (Transfer& t : sh.ts) {
         if ((st = normalise_rows(t)) != PL_OK)
             return st;
-        total_bytes += t.count * S;
-    }
-
-    // One-row copy plans the bulk ring will move (the rule of
-    // pl_collective: forced, or automatic for plans moving at least
-    // kBulkAutoBytes whose regions are 16-byte aligned or that write at
-    // least twice what they read) stream best in items that move about
-    // kBulkItemBytes (measured on GB300: an AllGather at 1 GiB, one source
-    // and eight destinations, best with 64 KiB chunks; the MoE AllToAll,
-    // one and one, with 256 KiB).
-    bool bulk = pol.datapath == PL_ATOM_BULK || pol.datapath_auto;
-    bool all_aligned_regions = true;
-    uint64_t moved = 0, rd = 0, wr = 0, fanout = 2;
-    for (const Transfer& t : ts) {
-        bulk &= op == PL_COPY || t.srcs.size() == 1;
-        moved += t.count * S * (t.srcs.size() + t.dsts.size());
-        rd += t.count * S * t.srcs.size();
-        wr += t.count * S * t.dsts.size();
-        fanout = std::max<uint64_t>(fanout, t.srcs.size() + t.dsts.size());
+        sh.total_bytes += t.count * S;
+        sh.copy_like &= op == PL_COPY || t.srcs.size() == 1;
+        sh.moved += t.count * S * (t.srcs.size() + t.dsts.size());
+        sh.rd += t.count * S * t.srcs.size();
+        sh.wr += t.count * S * t.dsts.size();
+        sh.fanout = std::max<uint64_t>(sh.fanout, t.srcs.size() + t.dsts.size());
         for (const auto* side : {&t.srcs, &t.dsts})
             for (const Region& g : *side) {
-                bulk &= g.rows == 1;
-                all_aligned_regions &= (g.offset * S) % 16 == 0;
+                sh.one_row &= g.rows == 1;
+                sh.all_aligned_regions &= (g.offset * S) % 16 == 0;
+                sh.regions_aligned &= (g.offset * S) % 16 == 0 && (g.rows == 1 || (g.stride * S) % 16 == 0);
             }
+        sh.multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
+        sh.rs_shape &= t.srcs.size() > 1 && t.dsts.size() == 1;
+        sh.one_to_one &= t.srcs.size() == 1 && t.dsts.size() == 1;
     }
-    bulk &= pol.datapath == PL_ATOM_BULK ||
-            (moved >= kBulkAutoBytes && (all_aligned_regions || wr >= 2 * rd));
-    // Plans whose regions are all 16-byte aligned run the aligned kernels, the
-    // others the spliced ones, each with its own CTAs per SM.
-    bool regions_aligned = true;
-    for (const Transfer& t : ts)
+    for (const Transfer& t : sh.ts)
+        sh.equal &= t.count == sh.ts[0].count && t.srcs.size() == sh.ts[0].srcs.size() &&
+                    t.dsts.size() == sh.ts[0].dsts.size() && t.dsts[0].rows == 1;
+    return PL_OK;
+}
+
+// How the transfers are cut into work items (the automatic rules apply to
+// zero-staging lists whose items never wait on one another).
+enum class ChunkRule {
+    kFixed,   // equal chunks of chunk_elems (forced chunk size, staged and composed lists)
+    kInline,  // each transfer's share of the inline kernel's items, one item per CTA
+    kPerCta,  // small messages: each transfer's share of the grid, about one item per CTA
+    kEqual,   // near-equal items, a few per CTA
+    kGuided,  // guided self-scheduling: items shrink toward the end of the list
+};
+
+// The codesign policy of one plan.
+struct PlanPolicy {
+    bool staged = false;             // Stage -> Notify -> Consume through the scratch ring
+    bool ticketed = false;           // items wait on flags: claimed in index order
+    bool flagged_reduction = false;  // a list with flags that reduces: the two-CTA kernels
+    bool composed = false;           // reductions with several destinations: the Figure 6 form
+    bool bulk = false;               // copy items of one-row regions go through the bulk ring
+    int full_grid = 1;               // persistent grid for the plan's kernel class
+    ChunkRule rule = ChunkRule::kFixed;
+    uint64_t chunk_elems = 0;        // kFixed chunks (and the plan's reported chunk size)
+    uint64_t slot_elems = 0;         // one chunk plus a vector of alignment head
+    uint64_t slots_per_rank = 0;     // staged: slots in each rank's ring
+    uint64_t grain = 0;              // automatic chunk sizes are multiples of this many elements
+    std::vector<uint64_t> target;    // kInline / kPerCta / kEqual: elements per item of each transfer
+};
+
+// kInline: the inline-parameter form (the whole plan in the launch's
+// parameters, one item per CTA, no metadata loads) for zero-staging one-row
+// moves whose items and references fit the parameter block, every transfer's
+// destinations at one offset mod 16 bytes.  Each transfer gets its share of
+// kInlineMaxItems items by bytes moved, in multiples of the grain.  Regions
+// not all 16-byte aligned: items of at most kInlineMisalignedCopyVectors
+// (copies) or kInlineMisalignedReduceVectors (reductions) vectors (the
+// kernel's fastest loop, for larger items, wants aligned references).
+// Automatically: the ReduceScatter shape between aligned regions, or at most
+// kInlineAutoMoved bytes moved.  Returns whether the plan takes the form, with
+// the per-transfer item sizes in `target`.
+bool inline_targets(const PlanShape& sh, pl_op op, uint64_t grain, std::vector<uint64_t>& target)
+{
+    const uint64_t S = sh.S, E = sh.E;
+    bool fits = true;
+    uint64_t nitems = 0, nptrs = 0;
+    target.assign(sh.ts.size(), 0);
+    for (size_t i = 0; fits && i < sh.ts.size(); ++i) {
+        const Transfer& t = sh.ts[i];
         for (const auto* side : {&t.srcs, &t.dsts})
             for (const Region& g : *side)
-                regions_aligned &= (g.offset * S) % 16 == 0 && (g.rows == 1 || (g.stride * S) % 16 == 0);
-    const bool staged = pol.path == PL_PATH_STAGED;
-    bool multi_dst_sum = false;
-    for (const Transfer& t : ts)
-        multi_dst_sum |= op != PL_COPY && t.srcs.size() > 1 && t.dsts.size() > 1;
-    const bool ticketed = staged || (multi_dst_sum && pol.ar_form == PL_AR_COMPOSED);
+                fits &= g.rows == 1;
+        for (const Region& g : t.dsts)
+            fits &= (g.offset * S) % 16 == (t.dsts[0].offset * S) % 16;
+        fits &= t.dsts.size() <= (size_t)kMaxRanks && t.srcs.size() <= (size_t)kMaxRanks;
+        if (!fits || t.count == 0)
+            continue;
+        const uint64_t nref = t.srcs.size() + t.dsts.size();
+        const uint64_t share = std::max<uint64_t>(1, (uint64_t)kInlineMaxItems * (t.count * S * nref) / sh.moved);
+        uint64_t tg = (t.count + share - 1) / share;
+        tg = (tg + grain - 1) / grain * grain;
+        if (!sh.regions_aligned)
+            tg = std::min<uint64_t>(tg, misaligned_cap(op != PL_COPY && t.srcs.size() > 1, t.dsts.size()) * E);
+        fits &= tg * t.dsts.size() <= (1ull << 31);  // the kernel's 32-bit (vector, destination) index
+        target[i] = tg;
+        const uint64_t n = (t.count + tg - 1) / tg;
+        nitems += n;
+        nptrs += n * nref;
+    }
+    return fits && nitems <= (uint64_t)kInlineMaxItems && nptrs <= (uint64_t)kInlineMaxPtrs;
+}
+
+// Per-transfer item sizes: each transfer cut into `share(i)` near-equal items
+// in multiples of the grain, no smaller than `min_elems`.
+template <class Share>
+void share_targets(const PlanShape& sh, uint64_t grain, uint64_t min_elems, Share share, std::vector<uint64_t>& target)
+{
+    target.assign(sh.ts.size(), 0);
+    for (size_t i = 0; i < sh.ts.size(); ++i) {
+        if (sh.ts[i].count == 0)
+            continue;
+        const uint64_t n = share(sh.ts[i]);
+        uint64_t tg = (sh.ts[i].count + n - 1) / n;
+        target[i] = std::max(min_elems, (tg + grain - 1) / grain * grain);
+    }
+}
+
+// The automatic chunk rule of a zero-staging list whose items never wait on
+// one another.  A CTA moves its items one after another and each item starts
+// with a memory round trip that nothing overlaps, so:
+//  - small messages (at most kOneItemBytes per CTA) get about one item per
+//    CTA: each transfer is cut into its share of the grid;
+//  - larger ones whose transfers all have one size and fan-out, and aligned
+//    ones the bulk ring moves, are cut into k near-equal items per CTA (k =
+//    kItemsPerCta, or enough to keep chunks within the cap);
+//  - the others are cut by guided self-scheduling: each next item moves about
+//    remaining bytes / (kGuidedDiv x grid), so items shrink toward the end of
+//    the list, and CTAs that claim them in order as they finish end within one
+//    small item of each other, whatever the partition lengths.
+// Sizes are multiples of kChunkGrain bytes, so chunks after the first of a
+// row start as aligned as the row's aligned start.  (Strided transfers
+// balance better guided: measured.)
+void choose_auto_rule(const PlanShape& sh, pl_op op, const ResolvedPolicy& pol, PlanPolicy& pp)
+{
+    const uint64_t S = sh.S;
+    const uint64_t grid = (uint64_t)pp.full_grid;
+    const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && sh.moved > 0 &&
+                             (pol.datapath == PL_ATOM_INLINE ||
+                              (pol.datapath_auto && ((sh.rs_shape && sh.regions_aligned) || sh.moved <= kInlineAutoMoved)));
+    if (want_inline && inline_targets(sh, op, pp.grain, pp.target)) {
+        pp.rule = ChunkRule::kInline;
+        return;
+    }
+    if (sh.total_bytes / grid <= (sh.one_to_one ? kOneItemBytesOneToOne : kOneItemBytes)) {
+        pp.rule = ChunkRule::kPerCta;
+        const uint64_t min_elems = std::max(pp.grain, kMinChunkBytes / S / pp.grain * pp.grain);
+        share_targets(sh, pp.grain, min_elems, [&](const Transfer& t) {
+            return std::max<uint64_t>(1, grid * (t.count * S) / sh.total_bytes);
+        }, pp.target);
+        return;
+    }
+    if (sh.equal || (pp.bulk && sh.all_aligned_regions)) {
+        // k items per CTA, each transfer cut into floor(its share of k x grid)
+        // near-equal chunks: at most k items per CTA, none much larger than
+        // total / (k x grid).  On the bulk ring an item moves about
+        // kBulkItemBytes (measured on GB300: an AllGather at 1 GiB, one source
+        // and eight destinations, best with 64 KiB chunks; the MoE AllToAll,
+        // one and one, with 256 KiB).
+        pp.rule = ChunkRule::kEqual;
+        const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / sh.fanout, kBulkChunkMin), kBulkChunkMax);
+        const uint64_t cap = pp.bulk && sh.all_aligned_regions ? bulk_chunk : kMaxChunkBytes;
+        const uint64_t per_cta = (sh.total_bytes + grid - 1) / grid;
+        const uint64_t k = std::max<uint64_t>((per_cta + cap - 1) / cap, kItemsPerCta);
+        const uint64_t items = k * grid;
+        share_targets(sh, pp.grain, 0, [&](const Transfer& t) {
+            return std::max<uint64_t>(1, (uint64_t)((double)items * (double)(t.count * S) / (double)sh.total_bytes));
+        }, pp.target);
+        return;
+    }
+    pp.rule = ChunkRule::kGuided;
+}
+
+pl_status choose_policy(const PlanShape& sh, pl_op op, int R, const ResolvedPolicy& pol, int num_sms,
+                        Occupancy occ, uint64_t scratch_bytes, PlanPolicy& pp)
+{
+    const uint64_t S = sh.S, E = sh.E;
+    pp = PlanPolicy{};
+    // One-row copy plans the bulk ring will move: forced, or automatic for
+    // plans moving at least kBulkAutoBytes whose regions are 16-byte aligned or
+    // that write at least twice what they read (the rule of pl_collective).
+    pp.bulk = (pol.datapath == PL_ATOM_BULK || pol.datapath_auto) && sh.copy_like && sh.one_row &&
+              (pol.datapath == PL_ATOM_BULK ||
+               (sh.moved >= kBulkAutoBytes && (sh.all_aligned_regions || sh.wr >= 2 * sh.rd)));
+    pp.staged = pol.path == PL_PATH_STAGED;
+    pp.composed = pol.ar_form == PL_AR_COMPOSED;
+    pp.ticketed = pp.staged || (sh.multi_dst_sum && pp.composed);
     // Lists with flags that reduce (staged, composed) run the two-CTA kernels
     // even when aligned: their waits leave the single CTA's warps idle
     // (measured at 1 GiB: staged AllReduce 7.0 -> 5.9 ms, staged ReduceScatter
     // 5.6 -> 4.9 ms, composed AllReduce 3.25 -> 3.18 ms; staged copies lose:
-    // AllGather 2.5 -> 2.9 ms, so they keep one CTA).
-    hp.flagged_reduction = ticketed && op != PL_COPY;
-    // (The bulk ring's shared memory holds one CTA per SM, whatever the kernel.)
-    const int full_grid =
-        std::max(1, num_sms) *
-        std::max(1, (regions_aligned || bulk) && !hp.flagged_reduction ? occ.aligned : occ.spliced);
+    // AllGather 2.5 -> 2.9 ms, so they keep one CTA).  Plans whose regions are
+    // all 16-byte aligned run the aligned kernels, the others the spliced ones,
+    // each with its own CTAs per SM.  (The bulk ring's shared memory holds one
+    // CTA per SM, whatever the kernel.)
+    pp.flagged_reduction = pp.ticketed && op != PL_COPY;
+    pp.full_grid = std::max(1, num_sms) *
+                   std::max(1, (sh.regions_aligned || pp.bulk) && !pp.flagged_reduction ? occ.aligned : occ.spliced);
+    pp.grain = std::max<uint64_t>(E, kChunkGrain / S);
+
     uint64_t chunk_bytes = pol.chunk_bytes;
     if (chunk_bytes == 0) {
-        chunk_bytes = total_bytes / ((uint64_t)full_grid * kItemsPerCta);
+        chunk_bytes = sh.total_bytes / ((uint64_t)pp.full_grid * kItemsPerCta);
         chunk_bytes = std::min(std::max(chunk_bytes, kMinChunkBytes), kMaxChunkBytes);
     }
     chunk_bytes = std::max<uint64_t>(256, chunk_bytes / 256 * 256);
-
     // The staged path keeps chunks small, so that a ring of a given size holds
     // many rows of them (measured: the staged AllReduce does not gain from
     // larger chunks, the staged ReduceScatter loses).  The zero-staging
     // composed form takes the general rule (it gains from large chunks: at
     // 1 GiB, 256 KiB chunks ran at 0.68 of the roofline, 4 MiB at 0.79).
-    if (staged && pol.chunk_bytes == 0)
+    if (pp.staged && pol.chunk_bytes == 0) {
         chunk_bytes = std::min<uint64_t>(chunk_bytes, kTicketedChunkBytes);
-    if (staged && pol.chunk_bytes == 0) {
-        uint64_t per_rank = scratch_bytes / (uint64_t)R;
+        const uint64_t per_rank = scratch_bytes / (uint64_t)R;
         chunk_bytes = std::min(chunk_bytes, std::max<uint64_t>(256, per_rank / 4 / 256 * 256));
     }
-    const uint64_t chunk_elems = std::max<uint64_t>(E, chunk_bytes / S / E * E);
+    pp.chunk_elems = std::max<uint64_t>(E, chunk_bytes / S / E * E);
     // A slot holds one chunk; the first chunk of a row may carry up to one
     // vector more (the head that aligns the destination).
-    const uint64_t slot_elems = chunk_elems + E;
-    uint64_t slots_per_rank = 0;
-    if (staged) {
+    pp.slot_elems = pp.chunk_elems + E;
+    if (pp.staged) {
         // The ring of each rank holds at least 2 slots (a reducer re-stages
         // its result into its own ring while its inputs are still held).
-        uint64_t per_rank = scratch_bytes / (uint64_t)R;
-        slots_per_rank = per_rank / (slot_elems * S);
-        if (slots_per_rank < 2)
+        const uint64_t per_rank = scratch_bytes / (uint64_t)R;
+        pp.slots_per_rank = per_rank / (pp.slot_elems * S);
+        if (pp.slots_per_rank < 2)
             return PL_ERR_NOMEM;
         // A whole number of rows of one rank's stages, so that the stages a
         // rank makes in one row never wrap around its ring (they merge, below).
         std::vector<uint64_t> per_row(R, 0);
-        for (const Transfer& t : ts)
+        for (const Transfer& t : sh.ts)
             for (const Region& g : t.srcs)
                 ++per_row[g.rank];
         const uint64_t g = *std::max_element(per_row.begin(), per_row.end());
-        if (g > 1 && slots_per_rank >= 2 * g)
-            slots_per_rank = slots_per_rank / g * g;
+        if (g > 1 && pp.slots_per_rank >= 2 * g)
+            pp.slots_per_rank = pp.slots_per_rank / g * g;
     }
+    pp.rule = ChunkRule::kFixed;
+    if (!pp.ticketed && pol.chunk_bytes == 0)
+        choose_auto_rule(sh, op, pol, pp);
+    return PL_OK;
+}
 
-    std::vector<std::vector<Chunk>> chunks(ts.size());
-    std::vector<std::pair<size_t, size_t>> order;  // (transfer, chunk) in creation order
+// The chunks of every transfer and the order in which they are emitted:
+// (transfer, chunk) pairs, chunk c of every transfer before chunk c + 1,
+// except under guided scheduling, which emits chunks as it cuts them.
+struct Cuts {
+    std::vector<std::vector<Chunk>> chunks;
+    std::vector<std::pair<size_t, size_t>> order;
     size_t max_chunks = 0;
-    if (!ticketed && pol.chunk_bytes == 0) {
-        // Items that never wait on one another, automatic chunk size.  A CTA
-        // moves its items one after another and each item starts with a
-        // memory round trip that nothing overlaps, so:
-        //  - small messages (at most kOneItemBytes per CTA) get about one
-        //    item per CTA: each transfer is cut into its share of the grid;
-        //  - larger ones whose transfers all have one size and fan-out, and
-        //    aligned ones the bulk ring moves, are cut into equal chunks;
-        //  - the others are cut by guided self-scheduling: each next item
-        //    moves about remaining bytes / (kGuidedDiv x grid), so items
-        //    shrink toward the end of the list, and CTAs that claim them in
-        //    order as they finish (the claim rule below) end within one small
-        //    item of each other, whatever the partition lengths.  Transfers
-        //    take turns.
-        // Sizes are multiples of kChunkGrain bytes, so chunks after the first
-        // of a row start as aligned as the row's aligned start.
-        const uint64_t grain = std::max<uint64_t>(E, kChunkGrain / S);
-        auto round_grain = [&](uint64_t elems) { return std::max(grain, elems / grain * grain); };
-        std::vector<Cursor> cur(ts.size());
-        // One-row transfers of one size and fan-out cut into equal chunks are
-        // already balanced: about kItemsPerCta x grid items plus small row
-        // ends.  (Strided transfers balance better guided: measured.)
-        bool equal = true, one_to_one = true;
-        for (const Transfer& t : ts) {
-            equal &= t.count == ts[0].count && t.srcs.size() == ts[0].srcs.size() &&
-                     t.dsts.size() == ts[0].dsts.size() && t.dsts[0].rows == 1;
-            one_to_one &= t.srcs.size() == 1 && t.dsts.size() == 1;
-        }
-        const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / fanout, kBulkChunkMin), kBulkChunkMax);
-        // Inline-parameter form (the whole plan in the launch's parameters, one
-        // item per CTA, no metadata loads): zero-staging one-row moves whose
-        // items and references fit the parameter block, every transfer's
-        // destinations at one offset mod 16 bytes.  Each transfer gets its
-        // share of kInlineMaxItems items by bytes moved, in multiples of the
-        // grain.  Regions not all 16-byte aligned: items of at most
-        // kInlineMisalignedCopyVectors (copies) or kInlineMisalignedReduceVectors
-        // (reductions) vectors (the kernel's fastest loop, for larger items,
-        // wants aligned references).  Automatically: the
-        // ReduceScatter shape between aligned regions, or at most
-        // kInlineAutoMoved bytes moved.
-        std::vector<uint64_t> inline_target;
-        bool rs_shape = op != PL_COPY;
-        for (const Transfer& t : ts)
-            rs_shape &= t.srcs.size() > 1 && t.dsts.size() == 1;
-        const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && moved > 0 &&
-                                 (pol.datapath == PL_ATOM_INLINE ||
-                                  (pol.datapath_auto && ((rs_shape && regions_aligned) || moved <= kInlineAutoMoved)));
-        if (want_inline) {
-            bool fits = true;
-            uint64_t nitems = 0, nptrs = 0;
-            inline_target.assign(ts.size(), 0);
-            for (size_t i = 0; fits && i < ts.size(); ++i) {
-                const Transfer& t = ts[i];
-                for (const auto* side : {&t.srcs, &t.dsts})
-                    for (const Region& g : *side)
-                        fits &= g.rows == 1;
-                for (const Region& g : t.dsts)
-                    fits &= (g.offset * S) % 16 == (t.dsts[0].offset * S) % 16;
-                fits &= t.dsts.size() <= (size_t)kMaxRanks && t.srcs.size() <= (size_t)kMaxRanks;
-                if (!fits || t.count == 0)
-                    continue;
-                const uint64_t nref = t.srcs.size() + t.dsts.size();
-                const uint64_t share = std::max<uint64_t>(1, (uint64_t)kInlineMaxItems * (t.count * S * nref) / moved);
-                uint64_t target = (t.count + share - 1) / share;
-                target = (target + grain - 1) / grain * grain;
-                if (!regions_aligned)
-                    target = std::min<uint64_t>(target, misaligned_cap(op != PL_COPY && t.srcs.size() > 1,
-                                                                       t.dsts.size()) * E);
-                fits &= target * t.dsts.size() <= (1ull << 31);  // the kernel's 32-bit (vector, destination) index
-                inline_target[i] = target;
-                const uint64_t n = (t.count + target - 1) / target;
-                nitems += n;
-                nptrs += n * nref;
-            }
-            hp.inline_form = fits && nitems <= (uint64_t)kInlineMaxItems && nptrs <= (uint64_t)kInlineMaxPtrs;
-        }
-        if (hp.inline_form) {
-            for (size_t i = 0; i < ts.size(); ++i)
-                for (uint64_t left = ts[i].count; left > 0;) {
-                    const Chunk ch = next_chunk(ts[i], cur[i], inline_target[i], E);
-                    chunks[i].push_back(ch);
-                    left -= ch.nrows * ch.ncols;
-                }
-            for (auto& cs : chunks)
-                max_chunks = std::max(max_chunks, cs.size());
-            for (size_t c = 0; c < max_chunks; ++c)
-                for (size_t ti = 0; ti < ts.size(); ++ti)
-                    if (c < chunks[ti].size())
-                        order.push_back({ti, c});
-        } else if (total_bytes / (uint64_t)full_grid <= (one_to_one ? kOneItemBytesOneToOne : kOneItemBytes)) {
-            const uint64_t min_elems = round_grain(kMinChunkBytes / S);
-            for (size_t i = 0; i < ts.size(); ++i) {
-                if (ts[i].count == 0)
-                    continue;
-                const uint64_t share = std::max<uint64_t>(1, (uint64_t)full_grid * (ts[i].count * S) / total_bytes);
-                uint64_t target = (ts[i].count + share - 1) / share;
-                target = std::max(min_elems, (target + grain - 1) / grain * grain);
-                for (uint64_t left = ts[i].count; left > 0;) {
-                    const Chunk ch = next_chunk(ts[i], cur[i], target, E);
-                    chunks[i].push_back(ch);
-                    left -= ch.nrows * ch.ncols;
-                }
-            }
-            for (auto& cs : chunks)
-                max_chunks = std::max(max_chunks, cs.size());
-            for (size_t c = 0; c < max_chunks; ++c)
-                for (size_t ti = 0; ti < ts.size(); ++ti)
-                    if (c < chunks[ti].size())
-                        order.push_back({ti, c});
-        } else if (equal || (bulk && all_aligned_regions)) {
-            // k items per CTA (kItemsPerCta, or enough to keep chunks within
-            // the cap), each transfer cut into floor(its share of k x grid)
-            // near-equal chunks: at most k items per CTA, none much larger
-            // than total / (k x grid).
-            const uint64_t cap = bulk && all_aligned_regions ? bulk_chunk : kMaxChunkBytes;
-            const uint64_t per_cta = (total_bytes + (uint64_t)full_grid - 1) / (uint64_t)full_grid;
-            const uint64_t k = std::max<uint64_t>((per_cta + cap - 1) / cap, kItemsPerCta);
-            const uint64_t items = k * (uint64_t)full_grid;
-            for (size_t i = 0; i < ts.size(); ++i) {
-                if (ts[i].count == 0)
-                    continue;
-                const uint64_t share = std::max<uint64_t>(1, (uint64_t)((double)items * (double)(ts[i].count * S) /
-                                                                        (double)total_bytes));
-                uint64_t target = (ts[i].count + share - 1) / share;
-                target = (target + grain - 1) / grain * grain;
-                for (uint64_t left = ts[i].count; left > 0;) {
-                    const Chunk ch = next_chunk(ts[i], cur[i], target, E);
-                    chunks[i].push_back(ch);
-                    left -= ch.nrows * ch.ncols;
-                }
-                max_chunks = std::max(max_chunks, chunks[i].size());
-            }
-            for (size_t c = 0; c < max_chunks; ++c)
-                for (size_t ti = 0; ti < ts.size(); ++ti)
-                    if (c < chunks[ti].size())
-                        order.push_back({ti, c});
-        } else {
-            uint64_t rem_moved = 0;
-            std::vector<uint64_t> rem(ts.size()), w(ts.size());
-            for (size_t i = 0; i < ts.size(); ++i) {
-                rem[i] = ts[i].count;
-                w[i] = S * (ts[i].srcs.size() + ts[i].dsts.size());
-                rem_moved += rem[i] * w[i];
-            }
-            const uint64_t tail_bytes = std::min(std::max(total_bytes / ((uint64_t)full_grid * kGuidedTailDiv),
-                                                          kGuidedTailMin), kGuidedTailMax);
-            const uint64_t min_elems = round_grain(tail_bytes / S);
-            const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
-            for (size_t k = 0; rem_moved > 0; k = (k + 1) % ts.size()) {
-                if (rem[k] == 0)
-                    continue;
-                uint64_t target = rem_moved / ((uint64_t)full_grid * kGuidedDiv) / w[k];
-                target = std::min(std::max(round_grain(target), min_elems), max_elems);
-                const Chunk ch = next_chunk(ts[k], cur[k], target, E);
-                const uint64_t got = ch.nrows * ch.ncols;
-                chunks[k].push_back(ch);
-                order.push_back({k, chunks[k].size() - 1});
-                rem[k] -= got;
-                rem_moved -= got * w[k];
-            }
-            for (auto& cs : chunks)
-                max_chunks = std::max(max_chunks, cs.size());
-        }
+};
+
+void cut_guided(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
+{
+    const uint64_t S = sh.S, E = sh.E, grid = (uint64_t)pp.full_grid;
+    auto round_grain = [&](uint64_t elems) { return std::max(pp.grain, elems / pp.grain * pp.grain); };
+    std::vector<Cursor> cur(sh.ts.size());
+    uint64_t rem_moved = 0;
+    std::vector<uint64_t> rem(sh.ts.size()), w(sh.ts.size());
+    for (size_t i = 0; i < sh.ts.size(); ++i) {
+        rem[i] = sh.ts[i].count;
+        w[i] = S * (sh.ts[i].srcs.size() + sh.ts[i].dsts.size());
+        rem_moved += rem[i] * w[i];
+    }
+    const uint64_t tail_bytes =
+        std::min(std::max(sh.total_bytes / (grid * kGuidedTailDiv), kGuidedTailMin), kGuidedTailMax);
+    const uint64_t min_elems = round_grain(tail_bytes / S);
+    const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
+    // transfers take turns
+    for (size_t k = 0; rem_moved > 0; k = (k + 1) % sh.ts.size()) {
+        if (rem[k] == 0)
+            continue;
+        uint64_t target = rem_moved / (grid * kGuidedDiv) / w[k];
+        target = std::min(std::max(round_grain(target), min_elems), max_elems);
+        const Chunk ch = next_chunk(sh.ts[k], cur[k], target, E);
+        const uint64_t got = ch.nrows * ch.ncols;
+        cu.chunks[k].push_back(ch);
+        cu.order.push_back({k, cu.chunks[k].size() - 1});
+        rem[k] -= got;
+        rem_moved -= got * w[k];
+    }
+}
+
+Cuts cut_chunks(const PlanShape& sh, const PlanPolicy& pp)
+{
+    Cuts cu;
+    cu.chunks.resize(sh.ts.size());
+    if (pp.rule == ChunkRule::kGuided) {
+        cut_guided(sh, pp, cu);
     } else {
-        for (size_t i = 0; i < ts.size(); ++i) {
-            chunks[i] = make_chunks(ts[i], chunk_elems, E);
-            max_chunks = std::max(max_chunks, chunks[i].size());
+        for (size_t i = 0; i < sh.ts.size(); ++i) {
+            if (pp.rule == ChunkRule::kFixed) {
+                cu.chunks[i] = make_chunks(sh.ts[i], pp.chunk_elems, sh.E);
+                continue;
+            }
+            Cursor cur;
+            for (uint64_t left = sh.ts[i].count; left > 0;) {
+                const Chunk ch = next_chunk(sh.ts[i], cur, pp.target[i], sh.E);
+                cu.chunks[i].push_back(ch);
+                left -= ch.nrows * ch.ncols;
+            }
         }
-        // row by row: chunk c of every transfer, then chunk c + 1
-        for (size_t c = 0; c < max_chunks; ++c)
-            for (size_t ti = 0; ti < ts.size(); ++ti)
-                if (c < chunks[ti].size())
-                    order.push_back({ti, c});
+    }
+    for (auto& cs : cu.chunks)
+        cu.max_chunks = std::max(cu.max_chunks, cs.size());
+    if (pp.rule != ChunkRule::kGuided)
+        for (size_t c = 0; c < cu.max_chunks; ++c)
+            for (size_t ti = 0; ti < sh.ts.size(); ++ti)
+                if (c < cu.chunks[ti].size())
+                    cu.order.push_back({ti, c});
+    return cu;
+}
+
+// One item waiting to be emitted, with the chunk row and SNAC phase that
+// place it in claim order.
+struct Deferred {
+    Builder::Pending p;
+    ItemKind kind;
+    pl_op op;
+    Chunk ch;
+};
+
+// Items of the derivation, by chunk row and phase: 0 producers (zero-staging
+// moves, stages, the owner's reduce of the zero-staging composed form),
+// 1 consumers of staged chunks, 2 gathers of reduced chunks.  Without a lag
+// items are emitted at once, in creation order (each transfer's producers,
+// then its consumers).
+class Emitter {
+public:
+    Emitter(HostPlan& hp, const PlanShape& sh, const PlanPolicy& pp, pl_op op, int R, int lag, size_t rows)
+        : b(hp, R), sh_(sh), pp_(pp), op_(op), R_(R), lag_(lag), cursor_(R, 0)
+    {
+        for (auto& r : rows_)
+            r.assign(rows, {});
+        if (pp.staged)
+            uses_.assign((size_t)R * pp.slots_per_rank, 0);
     }
 
-    Builder b(hp, R);
-    struct Deferred {
-        Builder::Pending p;
-        ItemKind kind;
-        pl_op op;
-        Chunk ch;
-    };
-    // phase 0: producers (zero-staging moves, stages, owner reduce of the
-    // zero-staging composed form); phase 1: consumers of staged chunks;
-    // phase 2: gathers of reduced chunks.
-    std::vector<std::vector<Deferred>> rows[3];
+    pl_status chunk(const Transfer& t, size_t row, const Chunk& ch)
+    {
+        if (!pp_.staged) {
+            zero_staging(t, row, ch);
+            return PL_OK;
+        }
+        tickets = true;
+        return staged(t, row, ch);
+    }
+
+    void merge_stages();
+    int resolve_lag(size_t max_chunks) const;
+    void emit_in_lag_order(size_t max_chunks, int lag);
+
+    Builder b;
     bool tickets = false;
     uint32_t next_flag = 0;
-    // staged ring bookkeeping
-    std::vector<uint64_t> cursor(R, 0);
-    std::vector<uint32_t> uses;
-    if (staged)
-        uses.assign((size_t)R * slots_per_rank, 0);
     uint64_t bytes_read = 0, bytes_written = 0;
 
-    auto owner_of = [&](const Transfer& t) -> size_t {
+private:
+    void put(size_t row, int phase, Builder::Pending& pend, ItemKind kind, pl_op pop, const Chunk& ch)
+    {
+        if (lag_ == 0 || !pp_.ticketed)
+            b.emit(pend, kind, pop, ch);
+        else
+            rows_[phase][row].push_back(Deferred{std::move(pend), kind, pop, ch});
+    }
+
+    // The slot of the next chunk `rank` stages, and which use of that slot it is.
+    pl_status stage_slot(int rank, uint32_t& slot_out, uint32_t& use_out)
+    {
+        const uint64_t s = (uint64_t)rank * pp_.slots_per_rank + (cursor_[rank]++ % pp_.slots_per_rank);
+        if (uses_[s] >= kMaxUsesPerLaunch)
+            return PL_ERR_UNSUPPORTED;
+        slot_out = (uint32_t)s;
+        use_out = uses_[s]++;
+        return PL_OK;
+    }
+
+    // The destination whose rank owns the transfer's partition (Figure 6: rank
+    // k reduces partition k).
+    static size_t owner_of(const Transfer& t)
+    {
         for (size_t d = 0; d < t.dsts.size(); ++d)
             if ((uint64_t)t.dsts[d].rank == t.name)
                 return d;
         return 0;
-    };
+    }
 
-    auto stage = [&](int rank, uint32_t& slot_out, uint32_t& use_out) -> pl_status {
-        uint64_t s = (uint64_t)rank * slots_per_rank + (cursor[rank]++ % slots_per_rank);
-        if (uses[s] >= kMaxUsesPerLaunch)
-            return PL_ERR_UNSUPPORTED;
-        slot_out = (uint32_t)s;
-        use_out = uses[s]++;
+    void zero_staging(const Transfer& t, size_t row, const Chunk& ch);
+    pl_status staged(const Transfer& t, size_t row, const Chunk& ch);
+    void staged_composed(const Transfer& t, size_t row, const Chunk& ch, const std::vector<uint32_t>& slot,
+                         const std::vector<uint32_t>& use, uint32_t yslot, uint32_t yuse);
+
+    const PlanShape& sh_;
+    const PlanPolicy& pp_;
+    pl_op op_;
+    int R_;
+    int lag_;
+    std::vector<std::vector<Deferred>> rows_[3];
+    std::vector<uint64_t> cursor_;  // staged: chunks each rank has staged so far
+    std::vector<uint32_t> uses_;    // staged: uses of each slot so far
+};
+
+void Emitter::zero_staging(const Transfer& t, size_t row, const Chunk& ch)
+{
+    const uint64_t blk = ch.nrows * ch.ncols * sh_.S;
+    const bool sum = op_ != PL_COPY && t.srcs.size() > 1;  // a reduction (sum or maximum)
+    if (sum && t.dsts.size() > 1 && pp_.composed) {
+        // Figure 6, zero-staging: the owner reduces the chunk into its output
+        // and notifies; one item then reads the owner's chunk once and writes
+        // it to every other rank (an AllGather item).
+        tickets = true;
+        const size_t o = owner_of(t);
+        const uint32_t flag = next_flag++;
+        Builder::Pending red;
+        for (auto& g : t.srcs)
+            red.src.push_back(b.region(g, ch));
+        red.dst.push_back(b.region(t.dsts[o], ch));
+        red.posts.push_back(mk_sync(kNotify, flag, 0));
+        put(row, 0, red, kMove, op_, ch);
+        bytes_read += blk * t.srcs.size();
+        bytes_written += blk;
+        Builder::Pending ag;
+        ag.src.push_back(b.region(t.dsts[o], ch));
+        for (size_t d = 0; d < t.dsts.size(); ++d)
+            if (d != o)
+                ag.dst.push_back(b.region(t.dsts[d], ch));
+        ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
+        put(row, 2, ag, kConsume, PL_COPY, ch);
+        bytes_read += blk;
+        bytes_written += blk * (t.dsts.size() - 1);
+        return;
+    }
+    // Zero-staging Consume: read the sources, write every destination.
+    for (size_t d0 = 0; d0 < t.dsts.size(); d0 += kMaxRanks) {
+        Builder::Pending mv;
+        for (auto& g : t.srcs)
+            mv.src.push_back(b.region(g, ch));
+        const size_t d1 = std::min(t.dsts.size(), d0 + kMaxRanks);
+        for (size_t d = d0; d < d1; ++d)
+            mv.dst.push_back(b.region(t.dsts[d], ch));
+        put(row, 0, mv, kMove, op_, ch);
+        bytes_read += blk * t.srcs.size();
+        bytes_written += blk * (d1 - d0);
+    }
+}
+
+// Staged SNAC: every source rank stages its chunk into its ring and
+// notifies; consumers wait, copy or reduce from the ring, and credit the slot
+// so its producer may reuse it.
+pl_status Emitter::staged(const Transfer& t, size_t row, const Chunk& ch)
+{
+    const uint64_t blk = ch.nrows * ch.ncols * sh_.S;
+    const uint64_t se = pp_.slot_elems;
+    const bool sum = op_ != PL_COPY && t.srcs.size() > 1;
+    pl_status st;
+    std::vector<uint32_t> slot(t.srcs.size()), use(t.srcs.size());
+    for (size_t s = 0; s < t.srcs.size(); ++s) {
+        if ((st = stage_slot(t.srcs[s].rank, slot[s], use[s])) != PL_OK)
+            return st;
+        Builder::Pending sg;
+        sg.src.push_back(b.region(t.srcs[s], ch));
+        sg.dst.push_back(b.slot(slot[s], se, ch));
+        if (use[s] > 0)
+            sg.waits.push_back(mk_sync(kWaitFree, slot[s], use[s] - 1));
+        sg.posts.push_back(mk_sync(kNotify, slot[s], use[s]));
+        put(row, 0, sg, kStage, PL_COPY, ch);
+        bytes_read += blk;
+        bytes_written += blk;
+    }
+    if (!sum) {
+        // COPY: one consumer per destination rank, each reading the slot.
+        const uint32_t n = (uint32_t)t.dsts.size();
+        for (size_t d = 0; d < t.dsts.size(); ++d) {
+            Builder::Pending cs;
+            cs.src.push_back(b.slot(slot[0], se, ch));
+            cs.dst.push_back(b.region(t.dsts[d], ch));
+            cs.waits.push_back(mk_sync(kWaitFull, slot[0], use[0]));
+            cs.posts.push_back(mk_sync(kCredit, slot[0], use[0], n));
+            put(row, 1, cs, kConsume, PL_COPY, ch);
+            bytes_read += blk;
+            bytes_written += blk;
+        }
         return PL_OK;
-    };
+    }
+    if (t.dsts.size() == 1 || !pp_.composed) {
+        // SUM: one consumer reduces the R staged chunks into every destination.
+        Builder::Pending cs;
+        for (size_t s = 0; s < t.srcs.size(); ++s)
+            cs.src.push_back(b.slot(slot[s], se, ch));
+        for (auto& g : t.dsts)
+            cs.dst.push_back(b.region(g, ch));
+        for (size_t s = 0; s < t.srcs.size(); ++s) {
+            cs.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
+            cs.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
+        }
+        put(row, 1, cs, kConsume, op_, ch);
+        bytes_read += blk * t.srcs.size();
+        bytes_written += blk * t.dsts.size();
+        return PL_OK;
+    }
+    // Figure 6: the owner reduces, writes its output and re-stages the reduced
+    // chunk into its own ring; the other ranks gather it.
+    const size_t o = owner_of(t);
+    uint32_t yslot, yuse;
+    if ((st = stage_slot(t.dsts[o].rank, yslot, yuse)) != PL_OK)
+        return st;
+    Builder::Pending red;
+    for (size_t s = 0; s < t.srcs.size(); ++s)
+        red.src.push_back(b.slot(slot[s], se, ch));
+    red.dst.push_back(b.region(t.dsts[o], ch));
+    red.dst.push_back(b.slot(yslot, se, ch));
+    for (size_t s = 0; s < t.srcs.size(); ++s)
+        red.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
+    if (yuse > 0)
+        red.waits.push_back(mk_sync(kWaitFree, yslot, yuse - 1));
+    for (size_t s = 0; s < t.srcs.size(); ++s)
+        red.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
+    red.posts.push_back(mk_sync(kNotify, yslot, yuse));
+    put(row, 1, red, kConsume, op_, ch);
+    bytes_read += blk * t.srcs.size();
+    bytes_written += 2 * blk;
+    const uint32_t n = (uint32_t)t.dsts.size() - 1;
+    for (size_t d = 0; d < t.dsts.size(); ++d) {
+        if (d == o)
+            continue;
+        Builder::Pending ag;
+        ag.src.push_back(b.slot(yslot, se, ch));
+        ag.dst.push_back(b.region(t.dsts[d], ch));
+        ag.waits.push_back(mk_sync(kWaitFull, yslot, yuse));
+        ag.posts.push_back(mk_sync(kCredit, yslot, yuse, n));
+        put(row, 2, ag, kConsume, PL_COPY, ch);
+        bytes_read += blk;
+        bytes_written += blk;
+    }
+    return PL_OK;
+}
 
-    for (auto& r : rows)
-        r.assign(max_chunks, {});
-    auto put = [&](size_t row, int phase, Builder::Pending& pend, ItemKind kind, pl_op pop, const Chunk& ch) {
-        if (lag == 0 || !ticketed)
-            b.emit(pend, kind, pop, ch);  // creation order: each transfer's producers, then its consumers
-        else
-            rows[phase][row].push_back(Deferred{std::move(pend), kind, pop, ch});
-    };
-    for (const auto& oc : order) {
-        {
-            const size_t ti = oc.first, c = oc.second;
-            const Transfer& t = ts[ti];
-            const Chunk& ch = chunks[ti][c];
-            const uint64_t blk = ch.nrows * ch.ncols * S;
-            const bool sum = op != PL_COPY && t.srcs.size() > 1;  // a reduction (sum or maximum)
-
-            if (!staged) {
-                if (sum && t.dsts.size() > 1 && pol.ar_form == PL_AR_COMPOSED) {
-                    // Figure 6, zero-staging: the owner reduces the chunk into its
-                    // output and notifies; one item then copies it to every other rank.
-                    tickets = true;
-                    size_t o = owner_of(t);
-                    uint32_t flag = next_flag++;
-                    Builder::Pending red;
-                    for (auto& g : t.srcs)
-                        red.src.push_back(b.region(g, ch));
-                    red.dst.push_back(b.region(t.dsts[o], ch));
-                    red.posts.push_back(mk_sync(kNotify, flag, 0));
-                    put(c, 0, red, kMove, op, ch);
-                    bytes_read += blk * t.srcs.size();
-                    bytes_written += blk;
-                    // The gather: one item reads the owner's chunk once and
-                    // writes it to every other rank (an AllGather item).
-                    Builder::Pending ag;
-                    ag.src.push_back(b.region(t.dsts[o], ch));
-                    for (size_t d = 0; d < t.dsts.size(); ++d)
-                        if (d != o)
-                            ag.dst.push_back(b.region(t.dsts[d], ch));
-                    ag.waits.push_back(mk_sync(kWaitFull, flag, 0));
-                    put(c, 2, ag, kConsume, PL_COPY, ch);
-                    bytes_read += blk;
-                    bytes_written += blk * (t.dsts.size() - 1);
-                } else {
-                    // Zero-staging Consume: read the sources, write every destination.
-                    for (size_t d0 = 0; d0 < t.dsts.size(); d0 += kMaxRanks) {
-                        Builder::Pending mv;
-                        for (auto& g : t.srcs)
-                            mv.src.push_back(b.region(g, ch));
-                        size_t d1 = std::min(t.dsts.size(), d0 + kMaxRanks);
-                        for (size_t d = d0; d < d1; ++d)
-                            mv.dst.push_back(b.region(t.dsts[d], ch));
-                        put(c, 0, mv, kMove, op, ch);
-                        bytes_read += blk * t.srcs.size();
-                        bytes_written += blk * (d1 - d0);
-                    }
-                }
+// Staged fused AllReduce (every transfer has as many destinations as
+// sources): the stages one source rank makes in one chunk row (its chunk of
+// each partition, equally spaced in its buffer, into consecutive slots of its
+// ring) become one multi-row item, which moves as many bytes as a consume
+// item: at R = 8 a row of 64 stage items and 8 consume items becomes 8 and 8
+// (measured 7% faster).  Where consume items are lighter (ReduceScatter: 8
+// sources, 1 destination) or re-stage (the composed form), merged stages
+// measured 8-11% slower, so they stay one per chunk.
+void Emitter::merge_stages()
+{
+    bool merge = pp_.staged && lag_ != 0 && !pp_.composed;
+    for (const Transfer& t : sh_.ts)
+        merge &= t.dsts.size() == t.srcs.size();
+    if (!merge)
+        return;
+    for (auto& row : rows_[0]) {
+        std::vector<Deferred> merged;
+        merged.reserve(row.size());
+        std::vector<bool> used(row.size(), false);
+        for (size_t i = 0; i < row.size(); ++i) {
+            if (used[i])
                 continue;
-            }
-
-            // Staged SNAC: every source rank stages its chunk into its ring and
-            // notifies; consumers wait, copy or reduce from the ring, and credit
-            // the slot so its producer may reuse it.
-            tickets = true;
-            std::vector<uint32_t> slot(t.srcs.size()), use(t.srcs.size());
-            for (size_t s = 0; s < t.srcs.size(); ++s) {
-                if ((st = stage(t.srcs[s].rank, slot[s], use[s])) != PL_OK)
-                    return st;
-                Builder::Pending sg;
-                sg.src.push_back(b.region(t.srcs[s], ch));
-                sg.dst.push_back(b.slot(slot[s], slot_elems, ch));
-                if (use[s] > 0)
-                    sg.waits.push_back(mk_sync(kWaitFree, slot[s], use[s] - 1));
-                sg.posts.push_back(mk_sync(kNotify, slot[s], use[s]));
-                put(c, 0, sg, kStage, PL_COPY, ch);
-                bytes_read += blk;
-                bytes_written += blk;
-            }
-            if (!sum) {
-                // COPY: one consumer per destination rank, each reading the slot.
-                uint32_t n = (uint32_t)t.dsts.size();
-                for (size_t d = 0; d < t.dsts.size(); ++d) {
-                    Builder::Pending cs;
-                    cs.src.push_back(b.slot(slot[0], slot_elems, ch));
-                    cs.dst.push_back(b.region(t.dsts[d], ch));
-                    cs.waits.push_back(mk_sync(kWaitFull, slot[0], use[0]));
-                    cs.posts.push_back(mk_sync(kCredit, slot[0], use[0], n));
-                    put(c, 1, cs, kConsume, PL_COPY, ch);
-                    bytes_read += blk;
-                    bytes_written += blk;
-                }
-            } else if (t.dsts.size() == 1 || pol.ar_form == PL_AR_FUSED) {
-                // SUM: one consumer reduces the R staged chunks into every destination.
-                Builder::Pending cs;
-                for (size_t s = 0; s < t.srcs.size(); ++s)
-                    cs.src.push_back(b.slot(slot[s], slot_elems, ch));
-                for (auto& g : t.dsts)
-                    cs.dst.push_back(b.region(g, ch));
-                for (size_t s = 0; s < t.srcs.size(); ++s) {
-                    cs.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
-                    cs.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
-                }
-                put(c, 1, cs, kConsume, op, ch);
-                bytes_read += blk * t.srcs.size();
-                bytes_written += blk * t.dsts.size();
-            } else {
-                // Figure 6: the owner reduces, writes its output and re-stages the
-                // reduced chunk into its own ring; the other ranks gather it.
-                size_t o = owner_of(t);
-                uint32_t yslot, yuse;
-                if ((st = stage(t.dsts[o].rank, yslot, yuse)) != PL_OK)
-                    return st;
-                Builder::Pending red;
-                for (size_t s = 0; s < t.srcs.size(); ++s)
-                    red.src.push_back(b.slot(slot[s], slot_elems, ch));
-                red.dst.push_back(b.region(t.dsts[o], ch));
-                red.dst.push_back(b.slot(yslot, slot_elems, ch));
-                for (size_t s = 0; s < t.srcs.size(); ++s)
-                    red.waits.push_back(mk_sync(kWaitFull, slot[s], use[s]));
-                if (yuse > 0)
-                    red.waits.push_back(mk_sync(kWaitFree, yslot, yuse - 1));
-                for (size_t s = 0; s < t.srcs.size(); ++s)
-                    red.posts.push_back(mk_sync(kCredit, slot[s], use[s], 1));
-                red.posts.push_back(mk_sync(kNotify, yslot, yuse));
-                put(c, 1, red, kConsume, op, ch);
-                bytes_read += blk * t.srcs.size();
-                bytes_written += 2 * blk;
-                uint32_t n = (uint32_t)t.dsts.size() - 1;
-                for (size_t d = 0; d < t.dsts.size(); ++d) {
-                    if (d == o)
+            used[i] = true;
+            Deferred d = std::move(row[i]);
+            if (d.kind == kStage && d.ch.nrows == 1 && d.p.src.size() == 1 && d.p.dst.size() == 1) {
+                const Ref s0 = d.p.src[0], d0 = d.p.dst[0];
+                uint64_t ss = 0, ds = 0, n = 1;
+                for (size_t j = i + 1; j < row.size(); ++j) {
+                    if (used[j])
                         continue;
-                    Builder::Pending ag;
-                    ag.src.push_back(b.slot(yslot, slot_elems, ch));
-                    ag.dst.push_back(b.region(t.dsts[d], ch));
-                    ag.waits.push_back(mk_sync(kWaitFull, yslot, yuse));
-                    ag.posts.push_back(mk_sync(kCredit, yslot, yuse, n));
-                    put(c, 2, ag, kConsume, PL_COPY, ch);
-                    bytes_read += blk;
-                    bytes_written += blk;
+                    const Deferred& e = row[j];
+                    if (e.kind != kStage || e.ch.nrows != 1 || e.ch.ncols != d.ch.ncols || e.p.src.size() != 1 ||
+                        e.p.dst.size() != 1 || e.p.src[0].buf != s0.buf || e.p.dst[0].buf != d0.buf)
+                        continue;
+                    const Ref& se = e.p.src[0];
+                    const Ref& de = e.p.dst[0];
+                    if (se.offset <= s0.offset || de.offset <= d0.offset)
+                        break;
+                    const uint64_t sse = (se.offset - s0.offset) / n, dse = (de.offset - d0.offset) / n;
+                    if (n == 1) {
+                        ss = sse;
+                        ds = dse;
+                    }
+                    if (sse != ss || dse != ds || ss * n != se.offset - s0.offset || ds * n != de.offset - d0.offset ||
+                        ss < d.ch.ncols || ds < d.ch.ncols)
+                        break;
+                    used[j] = true;
+                    ++n;
+                    for (const Sync& w : e.p.waits)
+                        d.p.waits.push_back(w);
+                    for (const Sync& q : e.p.posts)
+                        d.p.posts.push_back(q);
+                }
+                if (n > 1) {
+                    d.p.src[0].stride = ss;
+                    d.p.dst[0].stride = ds;
+                    d.ch = Chunk{0, n, 0, d.ch.ncols};
                 }
             }
+            merged.push_back(std::move(d));
         }
+        row = std::move(merged);
     }
+}
 
-    // Staged fused AllReduce (every transfer has as many destinations as
-    // sources): the stages one source rank makes in one chunk row (its chunk
-    // of each partition, equally spaced in its buffer, into consecutive slots
-    // of its ring) become one multi-row item, which moves as many bytes as a
-    // consume item: at R = 8 a row of 64 stage items and 8 consume items
-    // becomes 8 and 8 (measured 7% faster).  Where consume items are lighter
-    // (ReduceScatter: 8 sources, 1 destination) or re-stage (the composed
-    // form), merged stages measured 8-11% slower, so they stay one per chunk.
-    bool merge_stages = staged && lag != 0 && pol.ar_form != PL_AR_COMPOSED;
-    for (const Transfer& t : ts)
-        merge_stages &= t.dsts.size() == t.srcs.size();
-    if (merge_stages) {
-        for (auto& row : rows[0]) {
-            std::vector<Deferred> merged;
-            merged.reserve(row.size());
-            std::vector<bool> used(row.size(), false);
-            for (size_t i = 0; i < row.size(); ++i) {
-                if (used[i])
-                    continue;
-                used[i] = true;
-                Deferred d = std::move(row[i]);
-                if (d.kind == kStage && d.ch.nrows == 1 && d.p.src.size() == 1 && d.p.dst.size() == 1) {
-                    const Ref s0 = d.p.src[0], d0 = d.p.dst[0];
-                    uint64_t ss = 0, ds = 0, n = 1;
-                    for (size_t j = i + 1; j < row.size(); ++j) {
-                        if (used[j])
-                            continue;
-                        const Deferred& e = row[j];
-                        if (e.kind != kStage || e.ch.nrows != 1 || e.ch.ncols != d.ch.ncols || e.p.src.size() != 1 ||
-                            e.p.dst.size() != 1 || e.p.src[0].buf != s0.buf || e.p.dst[0].buf != d0.buf)
-                            continue;
-                        const Ref& se = e.p.src[0];
-                        const Ref& de = e.p.dst[0];
-                        if (se.offset <= s0.offset || de.offset <= d0.offset)
-                            break;
-                        const uint64_t sse = (se.offset - s0.offset) / n, dse = (de.offset - d0.offset) / n;
-                        if (n == 1) {
-                            ss = sse;
-                            ds = dse;
-                        }
-                        if (sse != ss || dse != ds || ss * n != se.offset - s0.offset || ds * n != de.offset - d0.offset ||
-                            ss < d.ch.ncols || ds < d.ch.ncols)
-                            break;
-                        used[j] = true;
-                        ++n;
-                        for (const Sync& w : e.p.waits)
-                            d.p.waits.push_back(w);
-                        for (const Sync& q : e.p.posts)
-                            d.p.posts.push_back(q);
-                    }
-                    if (n > 1) {
-                        d.p.src[0].stride = ss;
-                        d.p.dst[0].stride = ds;
-                        d.ch = Chunk{0, n, 0, d.ch.ncols};
-                    }
-                }
-                merged.push_back(std::move(d));
-            }
-            row = std::move(merged);
-        }
-    }
+// The lag in chunk rows between producers and their consumers.  The
+// automatic lag (a negative `lag_`) puts about two grids of producers between
+// a producer and its first consumer, so consumers are claimed once producers
+// are done.  (Counting the consumers of a row too made the lag shorter and the
+// composed AllReduce wait: 0.76 -> 0.49 of the roofline, measured.)
+int Emitter::resolve_lag(size_t max_chunks) const
+{
+    if (lag_ >= 0 || max_chunks == 0)
+        return lag_ < 0 ? 0 : lag_;
+    const size_t per_row = std::max<size_t>(1, rows_[0][0].size());
+    // CTAs hold claimed items ahead of the one they move, so about two grids
+    // of items may be claimed but not yet finished
+    return (int)std::min<size_t>(((size_t)2 * pp_.full_grid + per_row - 1) / per_row + 1, 64);
+}
 
-    // Emit: producers of row t, their consumers L rows later, gathers of
-    // reduced chunks one more lag later (or L when nothing sits between).
-    // The automatic lag puts about two grids of producers between a producer
-    // and its first consumer, so consumers are claimed once producers are done.
-    // (Counting the consumers of a row too made the lag shorter and the
-    // composed AllReduce wait: 0.76 -> 0.49 of the roofline, measured.)
-    if (lag < 0 && max_chunks > 0) {
-        size_t per_row = std::max<size_t>(1, rows[0][0].size());
-        // each CTA holds up to two claimed items, so about two grids of items
-        // may be claimed but not yet finished
-        lag = (int)std::min<size_t>(((size_t)2 * full_grid + per_row - 1) / per_row + 1, 64);
-    }
-    hp.lag = lag < 0 ? 0 : lag;
-    const size_t L = (size_t)hp.lag;
+// Emit in claim order: producers of row t, their consumers L rows later,
+// gathers of reduced chunks one more lag later (or L when nothing sits
+// between).
+void Emitter::emit_in_lag_order(size_t max_chunks, int lag)
+{
+    const size_t L = (size_t)lag;
     bool has_phase1 = false;
-    for (auto& r : rows[1])
+    for (auto& r : rows_[1])
         has_phase1 |= !r.empty();
     const size_t L2 = has_phase1 ? 2 * L : L;
     for (size_t t = 0; L > 0 && t < max_chunks + L2; ++t) {
         if (t < max_chunks)
-            for (Deferred& d : rows[0][t])
+            for (Deferred& d : rows_[0][t])
                 b.emit(d.p, d.kind, d.op, d.ch);
         if (t >= L && t - L < max_chunks)
-            for (Deferred& d : rows[1][t - L])
+            for (Deferred& d : rows_[1][t - L])
                 b.emit(d.p, d.kind, d.op, d.ch);
         if (t >= L2 && t - L2 < max_chunks)
-            for (Deferred& d : rows[2][t - L2])
+            for (Deferred& d : rows_[2][t - L2])
                 b.emit(d.p, d.kind, d.op, d.ch);
     }
+}
 
+// The plan's launch facts and statistics once its items exist: reference
+// layout, alignment, the kernel's op mix, the claim rule and grid.
+pl_status finalise_plan(HostPlan& hp, const PlanShape& sh, const PlanPolicy& pp, const ResolvedPolicy& pol,
+                        pl_op op, pl_dtype dt, bool tickets)
+{
+    const uint64_t S = sh.S, E = sh.E;
     if (hp.items.size() >= (1ull << 31) || hp.refs.size() >= (1ull << 32) || hp.syncs.size() >= (1ull << 32))
         return PL_ERR_UNSUPPORTED;
-    hp.nflags = staged ? (uint32_t)((uint64_t)R * slots_per_rank) : next_flag;
     // Items with one reference count, laid out in order: a CTA that knows its
     // first item's index loads that item's references alongside its header.
     if (!hp.items.empty()) {
@@ -1296,19 +1408,18 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     if (tickets && !waits_precede(hp))
         return PL_ERR_NOMEM;
 
-    int ctas = pol.ctas ? pol.ctas : full_grid;
+    int ctas = pol.ctas ? pol.ctas : pp.full_grid;
     ctas = (int)std::min<uint64_t>((uint64_t)ctas, std::max<uint64_t>(1, hp.items.size()));
     ctas = std::max(1, ctas);
     // Claim rule: items are claimed in index order through the device ticket
     // when they wait on one another, and also whenever there are more items
     // than CTAs, so that a CTA that finishes early takes the next item
-    // (dynamic balance; the guided sizes above rely on it).  One item per CTA
-    // needs no ticket.
+    // (dynamic balance; the guided sizes rely on it).  One item per CTA needs
+    // no ticket.
     const bool claim_in_order = tickets || hp.items.size() > (size_t)ctas;
-
     if (hp.inline_form && (hp.items.size() > (size_t)kInlineMaxItems || hp.refs.size() > (size_t)kInlineMaxPtrs))
-        hp.inline_form = false;  // (cannot happen: the cuts above are the items)
-    // Items within those vector counts run inline over buffers at any
+        hp.inline_form = false;  // (cannot happen: the inline cuts are the items)
+    // Items within the misaligned vector counts run inline over buffers at any
     // alignment (a destination head of up to E - 1 elements goes first).
     hp.inline_any_alignment = hp.inline_form;
     for (const Item& it : hp.items)
@@ -1318,17 +1429,51 @@ pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_d
     s.refs = hp.refs.size();
     s.syncs = hp.syncs.size();
     s.flags = hp.nflags;
-    s.chunk_elems = chunk_elems;
-    s.slots = slots_per_rank;
-    s.slot_elems = staged ? slot_elems : 0;
+    s.chunk_elems = pp.chunk_elems;
+    s.slots = pp.slots_per_rank;
+    s.slot_elems = pp.staged ? pp.slot_elems : 0;
     s.ctas = hp.inline_form ? (int)hp.items.size() : ctas;
     s.threads = hp.inline_form ? kInlineThreads : kThreads;
     s.uses_tickets = hp.inline_form ? 0 : (claim_in_order ? 1 : 0);
     s.path = pol.path;
-    s.bytes_read = bytes_read;
-    s.bytes_written = bytes_written;
     s.datapath = hp.inline_form ? PL_ATOM_INLINE : launch_bulk(hp, pol) ? PL_ATOM_BULK : PL_ATOM_VECTOR;
     return PL_OK;
+}
+
+// Derives the work list of a layout pair with consumers emitted `lag` chunk
+// rows behind the producers they wait for (so the CTAs that claim them in
+// order rarely spin); lag < 0 picks the automatic lag.
+pl_status derive_order(const pl_layout& in, const pl_layout& out, pl_op op, pl_dtype dt, int R,
+                       const ResolvedPolicy& pol, int num_sms, Occupancy occ, uint64_t scratch_bytes, int lag,
+                       HostPlan& hp)
+{
+    if (in.R != R || out.R != R)
+        return PL_ERR_INVALID;
+    hp = HostPlan{};
+    hp.R = R;
+    hp.dtype = dt;
+    PlanShape sh;
+    pl_status st = analyse(in, out, op, dt, R, sh);
+    if (st != PL_OK)
+        return st;
+    PlanPolicy pp;
+    if ((st = choose_policy(sh, op, R, pol, num_sms, occ, scratch_bytes, pp)) != PL_OK)
+        return st;
+    hp.flagged_reduction = pp.flagged_reduction;
+    hp.inline_form = pp.rule == ChunkRule::kInline;
+    const Cuts cu = cut_chunks(sh, pp);
+
+    Emitter em(hp, sh, pp, op, R, lag, cu.max_chunks);
+    for (const auto& oc : cu.order)
+        if ((st = em.chunk(sh.ts[oc.first], oc.second, cu.chunks[oc.first][oc.second])) != PL_OK)
+            return st;
+    em.merge_stages();
+    hp.lag = em.resolve_lag(cu.max_chunks);
+    em.emit_in_lag_order(cu.max_chunks, hp.lag);
+    hp.nflags = pp.staged ? (uint32_t)((uint64_t)R * pp.slots_per_rank) : em.next_flag;
+    hp.stats.bytes_read = em.bytes_read;
+    hp.stats.bytes_written = em.bytes_written;
+    return finalise_plan(hp, sh, pp, pol, op, dt, em.tickets);
 }
 
 // The work list of a layout pair: the automatic lag is tried first; a lag the
