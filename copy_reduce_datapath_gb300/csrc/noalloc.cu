@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 using namespace purlin;
 
@@ -39,38 +41,42 @@ static_assert((size_t)kMaxFlags * 20 + 64 <= kStateBytes, "flag words must fit t
 // Every GPU that loads the library holds this array until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
+// Host-side record of one device.  `list` is the host image of the work list
+// the device's array last received.  Its storage is reserved once for the
+// largest list and never moves or shrinks, so the copy that uploads it never
+// reads freed memory; a call whose work list equals it uploads nothing.
 struct DeviceSetup {
+    std::mutex mu;         // serialises set-up and uploads of this device
     char* base = nullptr;  // device address of g_noalloc_scratch on this device
     int num_sms = 0;
+    std::vector<unsigned char> list;
 };
 DeviceSetup g_setup[kMaxDevices];  // indexed by CUDA device ordinal (host side)
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Once per device, with that device current: the device address of the
-// static array (its name is only a host-side stand-in in host code).
-pl_status setup_device(int dev, DeviceSetup*& out)
+// Once per device, with that device current and d.mu held: the device
+// address of the static array (its name is only a host-side stand-in in host
+// code) and the SM count that sizes the grid.
+pl_status setup_device(int dev, DeviceSetup& d)
 {
-    if (dev < 0 || dev >= kMaxDevices)
-        return PL_ERR_INVALID;
-    DeviceSetup& d = g_setup[dev];
-    if (!d.base) {
-        void* ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return PL_ERR_CUDA;
-        }
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess || sms < 1) {
-            cudaGetLastError();
-            return PL_ERR_CUDA;
-        }
-        d.num_sms = sms;
-        d.base = static_cast<char*>(ptr);
+    if (d.base)
+        return PL_OK;
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return PL_ERR_CUDA;
     }
-    out = &d;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) {
+        cudaGetLastError();
+        return PL_ERR_CUDA;
+    }
+    d.list.reserve(kListBytes);
+    d.num_sms = sms;
+    d.base = static_cast<char*>(ptr);
     return PL_OK;
 }
 
@@ -93,8 +99,11 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
         cudaGetLastError();
         return PL_ERR_CUDA;
     }
-    DeviceSetup* d = nullptr;
-    pl_status st = setup_device(dev, d);
+    if (dev < 0 || dev >= kMaxDevices)
+        return PL_ERR_INVALID;
+    DeviceSetup* d = &g_setup[dev];
+    std::lock_guard<std::mutex> hold(d->mu);
+    pl_status st = setup_device(dev, *d);
     if (st != PL_OK)
         return st;
 
@@ -109,8 +118,10 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
     if (wl.nflags > kMaxFlags || os + bs > kListBytes || wl.items.empty())
         return PL_ERR_NOMEM;
 
-    // The work list goes into the array by one copy on the caller's stream; the
-    // flag words and counters must start at zero, so they are cleared first.
+    // The flag words and counters must start at zero: cleared on the caller's
+    // stream.  The work list goes into the array by one copy on that stream,
+    // from the device's host image, and only when it differs from the list the
+    // array already holds (the same AllReduce called again uploads nothing).
     std::vector<unsigned char> host(os + bs, 0);
     std::memcpy(host.data() + oi, wl.items.data(), bi);
     std::memcpy(host.data() + orr, wl.refs.data(), br);
@@ -118,8 +129,12 @@ extern "C" PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* list = d->base + kListOffset;
     cudaError_t e = cudaMemsetAsync(d->base, 0, kStateBytes, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(list, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && host != d->list) {
+        d->list.assign(host.begin(), host.end());  // within the reserved storage: no reallocation
+        e = cudaMemcpyAsync(list, d->list.data(), d->list.size(), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess)
+            d->list.clear();  // the array's list is unknown: upload again next time
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PL_ERR_CUDA;

@@ -267,12 +267,17 @@ PL_API pl_status pl_allreduce_op(pl_ctx* ctx, pl_op op, pl_dtype dtype, int R, u
  * The call works on the current CUDA device.  Its first call on a device also
  * looks up the array's device address there (cudaGetSymbolAddress); make that
  * first call before any stream capture.  Every call clears the array's flag
- * words and copies its work list into the array on `stream` before launching
- * one kernel there, so calls issued in order on one stream are safe, while
- * calls whose work overlaps on the GPU (other streams, other threads) share
- * the array and race.  wait = 0 returns once the work is queued; wait != 0
- * also waits for `stream` and returns the device status (PL_OK, or
- * PL_ERR_TIMEOUT if a bounded wait expired). */
+ * words on `stream` and launches one kernel there.  When its work list differs
+ * from the one the array holds (the first call, or a new R, count or dtype),
+ * it first copies the list into the array on `stream`, from a host image the
+ * library keeps per device; that copy is from pageable host memory, so the
+ * call waits for the work already queued on `stream` before it returns.  Calls issued in order on one stream are safe; calls whose work
+ * overlaps on the GPU (other streams, other host threads) share the array and
+ * race.  wait = 0 returns without waiting for the kernel and reports no device
+ * error: the next call clears the status word, so a bounded wait that expired
+ * in a wait = 0 call goes unreported.  wait != 0 also waits for `stream` and
+ * returns the device status (PL_OK, or PL_ERR_TIMEOUT if a bounded wait
+ * expired). */
 PL_API pl_status pl_allreduce_noalloc(pl_dtype dtype, int R, uint64_t count, void* const* in_bufs,
                                       void* const* out_bufs, int wait, void* stream);
 
