@@ -166,6 +166,43 @@ def pl_policy_default(**overrides) -> pl_policy:
     return p
 
 
+# ------------------------------------------------------------ owned handles
+
+
+class Handle(int):
+    """An opaque library handle: an int, as the C calls take it, that owns the
+    object behind it.  The object is freed by its destroy call or, failing
+    that, when the handle is garbage-collected; freeing twice is a no-op."""
+
+    _destroy_name = ""
+
+    def __new__(cls, value: int):
+        h = super().__new__(cls, value)
+        h._live = True
+        return h
+
+    def release(self) -> None:
+        if self._live:
+            self._live = False
+            _check(getattr(lib, self._destroy_name)(int(self)), self._destroy_name)
+
+    def __del__(self):
+        if getattr(self, "_live", False):
+            self._live = False
+            try:
+                getattr(lib, self._destroy_name)(int(self))
+            except Exception:  # interpreter shutdown: the library may be gone
+                pass
+
+
+class Layout(Handle):
+    _destroy_name = "pl_layout_destroy"
+
+
+class Plan(Handle):
+    _destroy_name = "pl_plan_destroy"
+
+
 # ---------------------------------------------------------------- layouts
 
 
@@ -182,11 +219,14 @@ def pl_layout_create(R: int, parts_per_rank) -> int:
     arr = (pl_part * max(1, len(flat)))(*flat)
     h = C.c_void_p()
     _check(lib.pl_layout_create(C.byref(h), R, counts, arr), "pl_layout_create")
-    return h.value
+    return Layout(h.value)
 
 
 def pl_layout_destroy(layout: int) -> None:
-    _check(lib.pl_layout_destroy(layout), "pl_layout_destroy")
+    if isinstance(layout, Handle):
+        layout.release()
+    else:
+        _check(lib.pl_layout_destroy(layout), "pl_layout_destroy")
 
 
 def pl_layout_info(layout: int):
@@ -199,7 +239,7 @@ def _builder(name):
     def make(R: int, lens) -> int:
         h = C.c_void_p()
         _check(getattr(lib, name)(C.byref(h), R, _u64s(lens)), name)
-        return h.value
+        return Layout(h.value)
     make.__name__ = name
     make.__doc__ = f"Calls {name}(R, lens) and returns the layout handle."
     return make
@@ -214,26 +254,26 @@ def pl_layout_alltoall_in(R: int, lens_matrix) -> int:
     h = C.c_void_p()
     _check(lib.pl_layout_alltoall_in(C.byref(h), R, _u64s([x for row in lens_matrix for x in row])),
            "pl_layout_alltoall_in")
-    return h.value
+    return Layout(h.value)
 
 
 def pl_layout_alltoall_out(R: int, lens_matrix) -> int:
     h = C.c_void_p()
     _check(lib.pl_layout_alltoall_out(C.byref(h), R, _u64s([x for row in lens_matrix for x in row])),
            "pl_layout_alltoall_out")
-    return h.value
+    return Layout(h.value)
 
 
 def pl_layout_ulysses_in(R: int, S: int, H: int, D: int) -> int:
     h = C.c_void_p()
     _check(lib.pl_layout_ulysses_in(C.byref(h), R, S, H, D), "pl_layout_ulysses_in")
-    return h.value
+    return Layout(h.value)
 
 
 def pl_layout_ulysses_out(R: int, S: int, H: int, D: int) -> int:
     h = C.c_void_p()
     _check(lib.pl_layout_ulysses_out(C.byref(h), R, S, H, D), "pl_layout_ulysses_out")
-    return h.value
+    return Layout(h.value)
 
 
 # ---------------------------------------------------------------- context
@@ -304,11 +344,14 @@ def pl_plan_create(in_layout, out_layout, op, dtype, R, policy: pl_policy | None
     _check(lib.pl_plan_create(C.byref(h), in_layout, out_layout, _op(op), _dtype(dtype), R,
                               C.byref(policy) if policy is not None else None, num_sms, scratch_bytes),
            "pl_plan_create")
-    return h.value
+    return Plan(h.value)
 
 
 def pl_plan_destroy(plan: int) -> None:
-    _check(lib.pl_plan_destroy(plan), "pl_plan_destroy")
+    if isinstance(plan, Handle):
+        plan.release()
+    else:
+        _check(lib.pl_plan_destroy(plan), "pl_plan_destroy")
 
 
 def pl_plan_get_stats(plan: int) -> pl_plan_stats:
