@@ -259,3 +259,60 @@ def test_max_special_values(ctx, dtype):
         assert gnan[4] and not gnan[5] and not gnan[6]
         keep = ~wnan
         assert_equal(g[keep], w[keep], f"rank {r}")
+
+
+# -------------------------------------------------- sums of special values
+
+
+def _nan_mask(a, dtype):
+    if dtype == "fp32":
+        return np.isnan(a)
+    f = oracle.f16_to_f32(a) if dtype == "fp16" else oracle.bf16_to_f32(a)
+    return np.isnan(f)
+
+
+@pytest.mark.parametrize("R", [3, 8])
+@pytest.mark.parametrize("pol", ["zs", "zs_small_chunks", "staged"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_sum_special_values(ctx, dtype, pol, R):
+    """The rank-ordered fp32 sum on NaN inputs, inf + (-inf), infinities and
+    sums that overflow: in the fp32 accumulation, or only at the final
+    rounding to bf16 / fp16 (a finite fp32 sum at or beyond the type's
+    rounding boundary to infinity).  NaN results are compared by position
+    only (the payload of a NaN produced by an addition or by a conversion is
+    not unique); every other element bit for bit.  Columns are tiled to
+    thousands of elements so that every launch form runs them."""
+    nan, inf = np.float32("nan"), np.float32("inf")
+    big = {"bf16": (np.float32(2.0 ** 127 * (2 - 2 ** -7)), np.float32(2.0 ** 119)),  # bf16 max + half an ulp
+           "fp16": (np.float32(65504.0), np.float32(16.0)),                           # fp16 max + half an ulp
+           "fp32": (np.float32(3e38), np.float32(3e38))}[dtype]
+    cols = [  # values of ranks 0, 1, 2; ranks 3.. add zeros
+        (nan, 1.0, 2.0), (1.0, nan, 2.0), (1.0, 2.0, nan), (inf, -inf, 0.0), (-inf, 1.0, inf),
+        (inf, 1.0, 2.0), (-inf, -inf, 1.0), (big[0], big[1], 0.0), (-big[0], -big[1], 0.0),
+        (1.0, 2.0, 3.0), (-0.0, -0.0, -0.0),
+    ]
+    reps = 1500
+    f32 = [np.tile(np.array([c[r] if r < 3 else 0.0 for c in cols], np.float32), reps) for r in range(R)]
+    if R > 3:  # a -0 column stays -0 only if every rank adds -0
+        for r in range(3, R):
+            f32[r][10::len(cols)] = -0.0
+    conv = {"bf16": oracle.f32_to_bf16, "fp16": oracle.f32_to_f16, "fp32": lambda a: a}[dtype]
+    ins = [conv(a) for a in f32]
+    n = ins[0].size
+    L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
+    got = run(ctx, L, L, "sum", dtype, ins, [n] * R, policies()[pol])
+    want = oracle.allreduce(ins, dtype)
+    nan_cols = np.zeros(len(cols), bool)
+    nan_cols[[0, 1, 2, 3, 4]] = True
+    expect_nan = np.tile(nan_cols, reps)
+    for r in range(R):
+        g, w = got[r], np.asarray(want[r])
+        gnan, wnan = _nan_mask(g, dtype), _nan_mask(w, dtype)
+        assert np.array_equal(wnan, expect_nan), "oracle: NaN positions"
+        assert np.array_equal(gnan, wnan), f"rank {r}: NaN positions"
+        keep = ~wnan
+        assert_equal(g[keep], w[keep], f"rank {r}")
+    # the overflow columns are infinite with the sign of their inputs
+    wf = np.asarray(want[0]).astype(np.float32) if dtype == "fp32" else \
+        (oracle.f16_to_f32 if dtype == "fp16" else oracle.bf16_to_f32)(np.asarray(want[0]))
+    assert np.isposinf(wf[7]) and np.isneginf(wf[8])

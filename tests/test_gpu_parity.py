@@ -384,3 +384,51 @@ def test_bulk_ring_in_flagged_paths(ctx, form):
         outs.check_guards()
         for r in range(R):
             assert_equal(outs.host(r), want[r], f"path {path} rank {r}")
+
+
+# ---------------------------------------------------- forced small grids
+
+
+@pytest.mark.parametrize("ctas", [8, 16, 32])
+@pytest.mark.parametrize("datapath,stages", [("vector", 0), ("bulk", 1), ("bulk", 8)])
+def test_forced_small_grids(ctx, ctas, datapath, stages):
+    """The grids and ring depths the depth x CTA sweep times: a few CTAs each
+    run many items in a row, so the bulk ring carries on from item to item
+    (aligned copies, copies realigned in shared memory and vector items in one
+    CTA), and reductions and copies share the claim order.  AllGatherV with
+    Zipf lengths (bf16 and one-byte elements), AllToAllV, ReduceScatterV and
+    AllReduce, each against the oracle."""
+    R = 8
+    pol = P.pl_policy_default(datapath=P.PL_ATOM_VECTOR if datapath == "vector" else P.PL_ATOM_BULK,
+                              stages=stages, ctas=ctas)
+    small = P.pl_policy_default(datapath=pol.datapath, stages=stages, ctas=ctas, chunk_bytes=16384)
+    for dtype, S in (("bf16", 2), ("fp8", 1)):
+        N = (4 << 20) // S + 13
+        lens = synth.zipf_lengths(N, R, 0.125, seed=60 + ctas)
+        ins = [host(None if dtype == "fp8" else "normal", dtype, 60, r, lens[r]) for r in range(R)]
+        want = oracle.allgather(ins, dtype)
+        for p in (pol, small):
+            got = run(ctx, P.pl_layout_rank_owned(R, lens), P.pl_layout_partitioned(R, lens), "copy", dtype, ins,
+                      [N] * R, p)
+            for r in range(R):
+                assert_equal(got[r], want[r], f"AGV {dtype} rank {r}")
+    dtype = "bf16"
+    N = (1 << 20) + 7
+    m = synth.zipf_matrix(N, R, 0.125, seed=61)
+    ains = [host("normal", dtype, 61, r, sum(m[r])) for r in range(R)]
+    outn = [sum(m[r][j] for r in range(R)) for j in range(R)]
+    want = oracle.alltoall(ains, m, dtype)
+    got = run(ctx, P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), "copy", dtype, ains, outn, pol)
+    for j in range(R):
+        assert_equal(got[j], want[j], f"A2AV rank {j}")
+    lens = synth.zipf_lengths(N, R, 0.125, seed=62)
+    rins = [host("normal", dtype, 62, r, N) for r in range(R)]
+    want = oracle.reducescatter(rins, lens, dtype)
+    got = run(ctx, P.pl_layout_partitioned(R, lens), P.pl_layout_rank_owned(R, lens), "sum", dtype, rins, lens, pol)
+    for k in range(R):
+        assert_equal(got[k], want[k], f"RSV rank {k}")
+    L = P.pl_layout_partitioned(R, synth.equal_lengths(N, R))
+    want = oracle.allreduce(rins, dtype)
+    got = run(ctx, L, L, "sum", dtype, rins, [N] * R, pol)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"AR rank {r}")
