@@ -109,6 +109,16 @@ def committed_traffic(kernel: str):
     return e.get("bytes_per_launch")
 
 
+def committed_traffic_note(kernel: str):
+    """How the committed DRAM traffic figure was taken (None when it is not
+    valid for the current kernel source)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if committed_traffic(kernel) is None:
+        return None
+    with open(p) as f:
+        return json.load(f)[kernel].get("note")
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
@@ -328,11 +338,19 @@ def sampled_parity(wl, device):
 SWEEP_OTHERS = ("reducescatter", "alltoall", "allgatherv", "reducescatterv", "alltoallv")
 
 
-def time_sweep(ctx, wl, stream, torch):
-    """Latency and algbw per size and collective (R = 8, bf16; V forms with
-    Zipf lengths).  Up to 64 MiB each point is a CUDA graph of `calls`
-    launches replayed on the launch stream (device time per call, no host
-    launch overhead); above that, events around back-to-back calls."""
+# Algorithmic HBM bytes of each swept collective at T bytes (per the T
+# convention of each: AllGather(V) output per rank, ReduceScatter(V) and
+# AllToAll(V) input per rank, AllReduce buffer per rank).
+SWEEP_MOVED = {"allgather": R + 1, "allreduce": 2 * R, "reducescatter": R + 1, "alltoall": 2 * R,
+               "allgatherv": R + 1, "reducescatterv": R + 1, "alltoallv": 2 * R}
+
+
+def time_sweep(ctx, wl, stream, torch, peak):
+    """Latency, algbw and fraction of the copy peak per size and collective
+    (R = 8, bf16; V forms with Zipf lengths).  Up to 64 MiB each point is a
+    CUDA graph of `calls` launches replayed on the launch stream (device time
+    per call, no host launch overhead); above that, events around back-to-back
+    calls."""
     out = []
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     for e in range(10, 31):
@@ -344,12 +362,10 @@ def time_sweep(ctx, wl, stream, torch):
             n = T // 2 // R if name == "allgather" else T // 2
             fn = getattr(wl, name)
             us, how = time_call(lambda: fn(ctx, stream.cuda_stream, n), T, stream, torch)
-            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how,
-                         "form": wl.sweep_form(name, T, sms)}
+            row[name] = point(us, T, SWEEP_MOVED[name] * T, peak, how, wl.sweep_form(name, T, sms))
         for name in SWEEP_OTHERS:
             us, how = time_call(wl.sweep_call(name, T, ctx, stream.cuda_stream), T, stream, torch)
-            row[name] = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2), "timed": how,
-                         "form": wl.sweep_form(name, T, sms)}
+            row[name] = point(us, T, SWEEP_MOVED[name] * T, peak, how, wl.sweep_form(name, T, sms))
         out.append(row)
     return out
 
@@ -384,6 +400,141 @@ def time_call(call, T, stream, torch):
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) * 1e3 / reps, "events"
+
+
+def plan_form(P, lin, lout, op, dtype, Rr, num_sms):
+    """The launch form the automatic policy takes for a layout pair (host-side
+    plan derivation; 16-byte aligned buffers)."""
+    plan = P.pl_plan_create(lin, lout, op, dtype, Rr, None, num_sms)
+    try:
+        st = P.pl_plan_get_stats(plan)
+    finally:
+        P.pl_plan_destroy(plan)
+    return {P.PL_ATOM_INLINE: "inline", P.PL_ATOM_BULK: "bulk", P.PL_ATOM_VECTOR: "vector"}.get(st.datapath, "?")
+
+
+def point(us, T, moved, peak, how, form=None):
+    """One timed point: latency, algbw (T / time), algorithmic HBM bandwidth
+    and its fraction of the copy peak."""
+    d = {"us": round(us, 3), "algbw_GBps": round(T / (us * 1e-6) / 1e9, 2),
+         "hbm_GBps": round(moved / (us * 1e-6) / 1e9, 1), "frac_of_peak": round(moved / (us * 1e-6) / 1e9 / peak, 4),
+         "timed": how}
+    if form:
+        d["form"] = form
+    return d
+
+
+def copy_engine_allgather(ins, outs, n):
+    """AllGather of n elements per rank by one device-to-device copy per
+    (source, destination) pair on the current stream: the copy-engine route,
+    which launches no kernel (the reference line beside the library's
+    AllGather kernel)."""
+    R_ = len(ins)
+    for r in range(R_):
+        for j in range(R_):
+            outs[r][j * n:(j + 1) * n].copy_(ins[j][:n], non_blocking=True)
+
+
+def time_configs(ctx, wl, stream, torch, peak):
+    """The other workloads of the benchmark's configuration list, timed by the
+    same rules as the sweep (graphs up to 64 MiB, events above), each with its
+    algorithmic bytes against the copy peak:
+      - three-rank fp32 AllReduce of integers in [-8, 8]: 3 x 4096 elements per
+        rank (latency), and scaled up to 1 GiB per rank;
+      - ReduceScatter, R = 8, fp32 and bf16 U(-1,1), T = 1 MiB .. 1 GiB per rank,
+        zero-staging out of place and in place (rank k's output is partition k
+        of its own input);
+      - AllToAll shaped like MoE token dispatch ([4096, 7168] bf16 per rank, 8
+        token groups) and the Ulysses sequence-to-head swap ([16384, 32, 128]
+        bf16 per rank);
+      - the copy-engine AllGather (one memcpy per source and destination pair,
+        no kernel) beside the library's AllGather at 64 MiB and 1 GiB.
+    The Zipf V forms are in the sweep."""
+    import synth
+    P = wl.P
+    dev = wl.ar_in[0].device
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    s = stream.cuda_stream
+    out = {}
+
+    # three ranks, fp32 integers
+    r3 = {}
+    for label, n in (("3x4096", 3 * 4096), ("1GiB", GiB // 4)):
+        ins = [synth.device_int_f32(0, r, n, dev) for r in range(3)]
+        outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+        L = P.pl_layout_partitioned(3, synth.equal_lengths(n, 3))
+        pi, po = P.ptrs(ins), P.ptrs(outs)
+        us, how = time_call(lambda: P.pl_allreduce(ctx, "fp32", 3, n, pi, po, None, s), n * 4, stream, torch)
+        r3[label] = point(us, n * 4, 2 * 3 * n * 4, peak, how, plan_form(P, L, L, "sum", "fp32", 3, sms))
+        P.pl_layout_destroy(L)
+        del ins, outs
+    out["allreduce_r3_fp32_int"] = r3
+
+    # ReduceScatter sweep, fp32 and bf16, out of place and in place
+    rs = []
+    for dt, tdt, S in (("fp32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        ins = [synth.device_uniform_pm1(2, r, GiB // S, dev, tdt) for r in range(R)]
+        outs = [torch.empty(GiB // S // R, dtype=tdt, device=dev) for _ in range(R)]
+        for e in range(20, 31):
+            T = 1 << e
+            N = T // S
+            lens = [N // R] * R
+            lin = P.pl_layout_partitioned(R, lens)
+            for variant in ("out_of_place", "in_place"):
+                if variant == "in_place":
+                    lout, po, cout = P.pl_layout_rank_owned_inplace(R, lens), P.ptrs(ins), [N] * R
+                else:
+                    lout, po, cout = P.pl_layout_rank_owned(R, lens), P.ptrs(outs), lens
+                pi = P.ptrs(ins)
+                call = lambda: P.pl_collective(ctx, lin, lout, "sum", dt, R, pi, [N] * R, po, cout, None, s)  # noqa: E731
+                us, how = time_call(call, T, stream, torch)
+                rs.append({"T": T, "dtype": dt, "variant": variant,
+                           **point(us, T, (R + 1) * T, peak, how, plan_form(P, lin, lout, "sum", dt, R, sms))})
+                P.pl_layout_destroy(lout)
+            P.pl_layout_destroy(lin)
+        del ins, outs
+    out["reducescatter"] = rs
+
+    # AllToAll: MoE token dispatch and the Ulysses swap
+    a2a = {}
+    n = 4096 * 7168
+    m = [[n // R] * R for _ in range(R)]
+    shapes = (("moe_4096x7168", P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), n),
+              ("ulysses_16384x32x128", P.pl_layout_ulysses_in(R, 16384, 32, 128),
+               P.pl_layout_ulysses_out(R, 16384, 32, 128), 16384 * 32 * 128))
+    for name, lin, lout, n in shapes:
+        ins = [synth.device_normal_bf16(3, r, n, dev) for r in range(R)]
+        outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        pi, po = P.ptrs(ins), P.ptrs(outs)
+        call = lambda: P.pl_collective(ctx, lin, lout, "copy", "bf16", R, pi, [n] * R, po, [n] * R, None, s)  # noqa: E731
+        us, how = time_call(call, n * 2, stream, torch)
+        a2a[name] = point(us, n * 2, 2 * R * n * 2, peak, how, plan_form(P, lin, lout, "copy", "bf16", R, sms))
+        P.pl_layout_destroy(lin)
+        P.pl_layout_destroy(lout)
+        del ins, outs
+    out["alltoall"] = a2a
+
+    # copy-engine AllGather against the kernel (the benchmark's AllGather buffers)
+    ce = []
+    for T in (64 << 20, wl.T):
+        n = T // 2 // R
+        ins, outs = wl.ag_in, wl.ag_out
+
+        def by_memcpy():
+            with torch.cuda.stream(stream):
+                copy_engine_allgather(ins, outs, n)
+        us_m, how_m = time_call(by_memcpy, T, stream, torch)
+        us_k, how_k = time_call(lambda: wl.allgather(ctx, s, n), T, stream, torch)
+        moved = (R + 1) * T
+        ce.append({"T": T, "memcpy_per_pair": point(us_m, T, moved, peak, how_m),
+                   "kernel": point(us_k, T, moved, peak, how_k, wl.sweep_form("allgather", T, sms))})
+    out["copy_engine_allgather"] = ce
+    out["note"] = ("points up to 64 MiB replay a CUDA graph on the same buffers back to back, so below the L2 size "
+                   "(129 MB of working set) they measure latency and L2 bandwidth, and frac_of_peak can exceed 1; "
+                   "from 128 MiB up, events around back-to-back calls on buffers larger than L2")
+    torch.cuda.synchronize()
+    assert P.pl_ctx_status(ctx, s) == P.PL_OK
+    return out
 
 
 def run_e2e(ctx, wl, stream, torch, steps):
@@ -613,13 +764,15 @@ def run_ours(args):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "algorithmic_bytes_per_launch": ar_bytes,
-                     "traffic": committed_traffic("allreduce_1GiB")},
+                     "traffic": committed_traffic("allreduce_1GiB"),
+                     "traffic_note": committed_traffic_note("allreduce_1GiB")},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "parity_sampled": parity_ok,
     }
     if rank == 0 and not args.no_sweep:
-        line["sweep"] = time_sweep(ctx, wl, stream, torch)
+        line["sweep"] = time_sweep(ctx, wl, stream, torch, peak)
+        line["configs"] = time_configs(ctx, wl, stream, torch, peak)
     if rank == 0 and not args.no_e2e:
         e2e = run_e2e(ctx, wl, stream, torch, args.e2e_steps)
         line["e2e"] = e2e
@@ -754,10 +907,18 @@ def run_case(args):
     assert P.pl_ctx_status(ctx, stream.cuda_stream) == P.PL_OK
     us = a.elapsed_time(b) * 1e3 / max(1, args.steps)
     peak, kind_peak = measured_peaks()
+    # The plan's own bytes (staging included), from the derived work list.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    scratch = args.scratch if pol.path == P.PL_PATH_STAGED else 0
+    plan = P.pl_plan_create(lin, lout, op, dt, Rr, pol, sms, scratch)
+    st = P.pl_plan_get_stats(plan)
+    own = int(st.bytes_read + st.bytes_written)
+    P.pl_plan_destroy(plan)
     print(json.dumps({"case": args.case, "workload": desc, "T_bytes": T, "policy": args.policy or "default",
-                      "scratch_bytes": args.scratch if pol.path == P.PL_PATH_STAGED else 0,
+                      "scratch_bytes": scratch,
                       "steps": args.steps, "us": round(us, 2), "algbw_GBps": round(T / us / 1e3, 2),
                       "hbm_GBps": round(moved / us / 1e3, 1), "frac_of_peak": round(moved / us / 1e3 / peak, 4),
+                      "plan_bytes": own, "plan_frac_of_peak": round(own / us / 1e3 / peak, 4),
                       "peak_GBps": peak, "peak_kind": kind_peak}), flush=True)
     P.pl_ctx_destroy(ctx)
 
@@ -938,7 +1099,10 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "AllGather + AllReduce over R=8 logical ranks, bf16 N(0,1) seed 1, equal "
                                f"partitions; each step a bounded sample of T={T_s >> 20} MiB per collective "
-                               "(the workload is T=1 GiB)", "R": R, "T_bytes": GiB},
+                               "(the workload is T=1 GiB)", "R": R, "T_bytes": T_s, "workload_T_bytes": GiB},
+        "steps_requested": args.steps,
+        "steps_note": f"the CPU oracle times at most 3 steps ({steps} timed of {args.steps} requested), so that "
+                      "the run ends within a few minutes",
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "single_thread_value": round(2 * T_s / dt1 / 1e9, 4),
                          "sample": f"T={T_s >> 20} MiB per collective, the C oracle on {cores} element-range "

@@ -214,3 +214,12 @@ def device_bytes(seed: int, rank: int, n: int, device):
     g = torch.Generator(device=device)
     g.manual_seed(device_seed(seed, rank))
     return torch.randint(0, 256, (n,), generator=g, device=device, dtype=torch.uint8)
+
+
+def device_int_f32(seed: int, rank: int, n: int, device, lo: int = -8, hi: int = 8):
+    """Integers uniform in [lo, hi] (inclusive) as fp32, drawn on ``device`` by
+    PyTorch's seeded generator (large inputs whose sums stay exact)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(device_seed(seed, rank))
+    return torch.randint(lo, hi + 1, (n,), generator=g, device=device, dtype=torch.int32).to(torch.float32)
