@@ -216,14 +216,19 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// At most n bulk groups of this thread still reading their shared memory (n < 8).
+// At most n bulk groups of this thread still reading their shared memory
+// (n >= 7 waits for at most 7).
 __device__ __forceinline__ void bulk_wait_read_n(int n)
 {
     switch (n) {
     case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
     case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
     case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
-    default: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory"); break;
     }
 }
 
@@ -249,6 +254,14 @@ __device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const Launch
 // barrier will complete next.  bulk_shift_copy (every thread) uses the same
 // buffers in pairs and its own barriers `sbar` with parities `sphase`, which
 // every thread keeps identically.
+//
+// Pieces are numbered across the items of the CTA (`gcopy` for bulk_copy,
+// `gshift` for bulk_shift_copy; each piece commits one bulk group of stores),
+// so that the ring runs on from one item into the next: an item that posts no
+// flags returns without waiting for its stores, which drain while the next
+// item's first loads are in flight, and the next item reuses a buffer only
+// once the stores that read it are done with it.  Switching between the two
+// functions (`mode`) first waits until every store has read the ring.
 struct BulkRing {
     char* buf;
     unsigned long long* bar;
@@ -256,16 +269,22 @@ struct BulkRing {
     unsigned phase;
     unsigned long long* sbar;
     unsigned sphase;
+    bool drain;       // the current item notifies or credits flags after its move
+    int mode;         // 0 none, 1 bulk_copy, 2 bulk_shift_copy: the last user of the ring
+    unsigned gcopy;   // thread 0: pieces bulk_copy has stored so far
+    unsigned gshift;  // every thread: pieces bulk_shift_copy has stored so far
 };
 
-// End of a bulk move: every store has landed, and the async-proxy stores are
-// ordered before the generic release that may follow.  (Waiting only until
-// the stores had read the ring, so that they overlap the next item's loads,
-// measured no faster.)
-__device__ __forceinline__ void bulk_finish()
+// End of a bulk move.  An item that posts flags waits until every store has
+// landed and orders the async-proxy stores before the generic release that
+// follows.  Any other item returns at once: nothing in the launch reads what
+// it wrote, and the kernel waits for all stores before it exits.
+__device__ __forceinline__ void bulk_finish(const BulkRing& bk)
 {
-    bulk_wait_all();
-    fence_proxy_async();
+    if (bk.drain) {
+        bulk_wait_all();
+        fence_proxy_async();
+    }
 }
 constexpr int kShiftMaxDepth = kBulkMaxStages / 2;
 
@@ -546,26 +565,38 @@ __device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigne
 // Thread 0: copies `nbytes` (a multiple of 16, both ends 16-byte aligned)
 // from `src` to every destination in `mask` through the ring.  Loads run up
 // to `stages` pieces ahead; a stage is refilled once the stores that read it
-// have finished reading.  Returns with every store complete.
+// have finished reading (stores of the previous items included: piece q of
+// this item is global piece G + q, in stage (G + q) mod stages).
 __device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long mask, unsigned row, size_t body,
                           const char* src, unsigned nbytes, const LaunchArgs& a)
 {
     const unsigned np = (nbytes + kBulkPiece - 1) / kBulkPiece;
     const unsigned st = (unsigned)bk.stages;
     fence_proxy_async();  // order earlier generic writes (after a flag acquire) before the async loads
+    if (bk.mode != 1) {
+        bulk_wait_read0();  // the ring was last used in pairs
+        bk.mode = 1;
+    }
+    const unsigned G = bk.gcopy;
     unsigned issued = 0;
     auto load = [&](unsigned q) {
-        const unsigned sidx = q % st;
+        const unsigned sidx = (G + q) % st;
         const unsigned bytes = min(kBulkPiece, nbytes - q * kBulkPiece);
         mbar_expect_tx(&bk.bar[sidx], bytes);
         bulk_g2s(bk.buf + (size_t)sidx * kBulkPiece, src + (size_t)q * kBulkPiece, bytes, &bk.bar[sidx]);
     };
-    for (; issued < np && issued < st; ++issued)
+    // The first loads reuse the stages of the previous item's last pieces:
+    // piece q waits until global piece G + q - st has read its stage (G groups
+    // committed, so at most st - 1 - q still reading).
+    for (; issued < np && issued < st; ++issued) {
+        if (G + issued >= st)
+            bulk_wait_read_n((int)(st - 1 - issued));
         load(issued);
+    }
     bool ok = true;
     unsigned p = 0;
     for (; p < np; ++p) {
-        const unsigned sidx = p % st;
+        const unsigned sidx = (G + p) % st;
         if (st == 1 && p >= 1) {
             bulk_wait_read0();
             load(p);
@@ -592,12 +623,14 @@ __device__ void bulk_copy(BulkRing& bk, const ItemShared& sh, unsigned long long
         // A load never completed in time: wait (bounded) for every load still in
         // flight so no copy lands in shared memory after this CTA moves on.
         for (unsigned q = p; q < issued; ++q) {
-            const unsigned sidx = q % st;
+            const unsigned sidx = (G + q) % st;
             if (mbar_wait(&bk.bar[sidx], (bk.phase >> sidx) & 1u, a))
                 bk.phase ^= 1u << sidx;
         }
+        bulk_wait_all();
     }
-    bulk_finish();
+    bk.gcopy = G + p;
+    bulk_finish(bk);
 }
 
 // Copy of nv output vectors from one source that sits q bytes (q != 0) past
@@ -621,11 +654,15 @@ __device__ void bulk_shift_copy(BulkRing& bk, const ItemShared& sh, unsigned lon
     constexpr unsigned kOut = kBulkPiece / 16 - 1;  // output vectors per piece
     const unsigned depth = (unsigned)bk.stages / 2;
     const unsigned np = (nv + kOut - 1) / kOut;
+    // Piece p of this item is global piece G + p, in pair (G + p) mod depth:
+    // the output buffer it realigns into was freed by the wait before the
+    // barrier of the previous piece, of this item or of the last one.
+    const unsigned G = bk.gshift;
     auto inb = [&](unsigned i) { return bk.buf + (size_t)(2 * i) * kBulkPiece; };
     auto outb = [&](unsigned i) { return bk.buf + (size_t)(2 * i + 1) * kBulkPiece; };
     auto nout_of = [&](unsigned p) { return min(kOut, nv - p * kOut); };
     auto load = [&](unsigned p) {
-        const unsigned i = p % depth;
+        const unsigned i = (G + p) % depth;
         const unsigned bytes = (nout_of(p) + 1u) * 16u;  // the last aligned vector still holds bytes of the row
         mbar_expect_tx(&bk.sbar[i], bytes);
         bulk_g2s(inb(i), src_al + (size_t)p * kOut * 16, bytes, &bk.sbar[i]);
@@ -633,12 +670,18 @@ __device__ void bulk_shift_copy(BulkRing& bk, const ItemShared& sh, unsigned lon
     unsigned issued = 0, waited = 0;  // thread 0's count of loads issued and of barrier waits passed
     if (tid == 0) {
         fence_proxy_async();  // earlier generic writes (after a flag acquire) before the async loads
+        if (bk.mode != 2)
+            bulk_wait_read0();  // the ring was last used as single stages
+        // Input buffers are free: every thread realigned from them before a
+        // barrier this thread has passed.
         for (; issued < np && issued < depth; ++issued)
             load(issued);
     }
+    bk.mode = 2;
     bool all_ok = true;
-    for (unsigned p = 0; p < np; ++p) {
-        const unsigned i = p % depth;
+    unsigned p = 0;
+    for (; p < np; ++p) {
+        const unsigned i = (G + p) % depth;
         const bool ok = mbar_wait(&bk.sbar[i], (bk.sphase >> i) & 1u, a);
         if (ok) {
             bk.sphase ^= 1u << i;
@@ -673,12 +716,15 @@ __device__ void bulk_shift_copy(BulkRing& bk, const ItemShared& sh, unsigned lon
     if (tid == 0) {
         // After a timeout, the loads still in flight land before the ring is reused.
         for (; !all_ok && waited < issued; ++waited) {
-            const unsigned i = waited % depth;
+            const unsigned i = (G + waited) % depth;
             if (mbar_wait(&bk.sbar[i], (bk.sphase >> i) & 1u, a))
                 bk.sphase ^= 1u << i;
         }
-        bulk_finish();
+        if (!all_ok)
+            bulk_wait_all();
+        bulk_finish(bk);
     }
+    bk.gshift = G + p;  // pieces whose stores were committed (every thread alike)
 }
 
 // Every source of the segment sits the same q bytes past a 16-byte boundary
@@ -1019,10 +1065,21 @@ struct __align__(16) Slot {
 
 // Thread 0: the next item index of this CTA (in index order through the
 // device ticket when items wait on one another or outnumber the CTAs, else
-// round-robin).
+// round-robin).  In lists without flags the item loops issue the claim of
+// item k+3 while item k moves and read its result only in the next
+// iteration, so the ticket's round trip (an atomic through L2, slow while the
+// memory system is saturated) does not hold up thread 0, and with it the CTA,
+// before a move.  Lists with flags claim item k+2 at the top of iteration k,
+// so that a CTA holds fewer items that later ones may wait for.
+// A list without flags (static_head) takes its first two items per CTA
+// statically, so that a CTA starts without a ticket round trip; in-order
+// claims only matter for later items (balance) and for lists whose items
+// wait on one another (progress), which claim every item by ticket.
 __device__ __forceinline__ unsigned claim(const LaunchArgs& a, unsigned k)
 {
-    return a.use_tickets ? atomicAdd(a.st.ticket, 1u) : blockIdx.x + k * gridDim.x;
+    if (!a.use_tickets || (a.static_head && k < 2))
+        return blockIdx.x + k * gridDim.x;
+    return atomicAdd(a.st.ticket, 1u) + (a.static_head ? 2u * gridDim.x : 0u);
 }
 
 // Asynchronous global -> shared copies (no registers held while in flight).
@@ -1062,8 +1119,11 @@ __device__ __forceinline__ bool put_ref(const LaunchArgs& a, const Item& it, con
 // region pointers in two ItemShared buffers (items k, k+1).
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared* sh, Slot* slot, Ref* sref, int* s_ok,
-                                                BulkRing& bk, int tid, bool bad, unsigned long long epoch)
+                                                BulkRing& bk, int tid, bool bad, unsigned long long epoch,
+                                                unsigned claimed)
 {
+    // `claimed` (thread 0, lists without flags): the index claimed for item
+    // k+2, ~0u once a claim has returned the end of the list.
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k % 3u), nxt = (int)((k + 1u) % 3u), nn = (int)((k + 2u) % 3u);
         const int scur = (int)(k & 1u), snxt = scur ^ 1;
@@ -1084,13 +1144,16 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
                 cp_async8(d + 16, g + 16);
             }
             if (tid == 0) {
-                const unsigned i2 = claim(a, k + 2);
+                const unsigned i2 = a.static_head ? claimed : claim(a, k + 2);
                 slot[nn].index = i2;
+                claimed = ~0u;
                 if (i2 < a.nitems) {
                     const char* g = reinterpret_cast<const char*>(a.items + i2);
                     char* d = reinterpret_cast<char*>(&slot[nn].item);
                     cp_async16(d, g);
                     cp_async16(d + 16, g + 16);
+                    if (a.static_head)
+                        claimed = claim(a, k + 3);  // read in the next iteration
                 }
             }
         } else if (tid == 0) {
@@ -1107,6 +1170,7 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
         const bool ok = *s_ok != 0;  // read by every thread before the next write (after the barrier below)
         if (ok) {
             const Item& it = slot[cur].item;
+            bk.drain = it.npost != 0;
             move_item<DT, OPS, BULK, true>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
         }
         cp_async_wait_all();
@@ -1128,13 +1192,26 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
 
 // Work-item loop of the spliced kernels (plans not proven aligned).  The
 // references of item k+1 and the header of item k+2 are loaded into
-// registers before item k moves and stored after it; at two CTAs per SM
+// registers while item k moves and stored after it; at two CTAs per SM
 // these kernels ran 1-2% faster this way than with the asynchronous copies
-// (which made the aligned kernels 1-3% faster).  Two header slots.
+// (which made the aligned kernels 1-3% faster).  Two header slots.  The
+// loads and the claim are issued after the barrier that starts the move, by
+// threads kPrefetchThread onwards: the move fills these kernels' 64
+// registers, so a value held across it may be spilled, and a spill waits for
+// its load (measured on GB300: 1.5-2 us per item when thread 0, which drives
+// the bulk ring, issued them before the barrier).  After the barrier that
+// wait overlaps the move's own first loads.
+constexpr int kPrefetchThread = 32;
+
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* sh, Slot* slot, int* s_ok,
-                                               BulkRing& bk, int tid, bool bad, unsigned long long epoch)
+                                               BulkRing& bk, int tid, bool bad, unsigned long long epoch,
+                                               unsigned* s_claimed)
 {
+    const int rt = tid - kPrefetchThread;  // the reference of the next item this thread loads
+    // `claimed` (thread kPrefetchThread, lists without flags): the index
+    // claimed for item k+2, ~0u once a claim has returned the end of the list.
+    unsigned claimed = tid == kPrefetchThread ? *s_claimed : ~0u;
     for (unsigned k = 0;; ++k) {
         const int cur = (int)(k & 1u), nxt = cur ^ 1;
         const unsigned index = slot[cur].index;
@@ -1142,18 +1219,6 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
             break;
         const Item it = slot[cur].item;
         const unsigned next_index = slot[nxt].index;
-        const Item nit = slot[nxt].item;
-        const bool has_ref = next_index < a.nitems && tid < nit.nsrc + nit.ndst;
-        Ref nref{};
-        if (has_ref)
-            nref = a.refs[nit.ref + tid];
-        unsigned i2 = ~0u;
-        Item h2{};
-        if (tid == 0 && next_index < a.nitems) {
-            i2 = claim(a, k + 2);
-            if (i2 < a.nitems)
-                h2 = a.items[i2];
-        }
         if (tid < 32) {
             const bool ok = it.nwait ? run_waits(a, it, tid, epoch) : true;
             if (tid == 0)
@@ -1162,12 +1227,29 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
         // `bad`: this thread's reference of item k is misaligned (put_ref)
         const bool proven = !__syncthreads_or(bad);
         const bool ok = *s_ok != 0;
+        const Item nit = slot[nxt].item;
+        const bool has_ref = next_index < a.nitems && rt >= 0 && rt < nit.nsrc + nit.ndst;
+        Ref nref{};
+        if (has_ref)
+            nref = a.refs[nit.ref + rt];
+        unsigned i2 = ~0u;
+        Item h2{};
+        if (tid == kPrefetchThread && next_index < a.nitems) {
+            i2 = a.static_head ? claimed : claim(a, k + 2);
+            claimed = ~0u;
+            if (i2 < a.nitems) {
+                h2 = a.items[i2];
+                if (a.static_head)
+                    claimed = claim(a, k + 3);  // read in the next iteration
+            }
+        }
+        bk.drain = it.npost != 0;
         if (ok)
             move_item<DT, OPS, BULK, false>(sh[cur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
         bad = false;
         if (has_ref)
-            bad = put_ref<DT>(a, nit, nref, sh[nxt], tid);  // sh[nxt] served item k-1, done before the last barrier
-        if (tid == 0) {
+            bad = put_ref<DT>(a, nit, nref, sh[nxt], rt);  // sh[nxt] served item k-1, done before the last barrier
+        if (tid == kPrefetchThread) {
             // every thread read slot[cur] and slot[nxt] before the barrier above
             slot[cur].index = i2;
             slot[cur].item = h2;
@@ -1178,11 +1260,13 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
     }
 }
 
-// The persistent SNAC kernel.  With tickets, a CTA holds at most two claimed
-// items and processes them in claim order; every wait of an item refers to
-// items with smaller indices, held by running CTAs, so the grid always
-// progresses.  A CTA claims item k+2 only while item k+1 exists, so every CTA
-// makes exactly one claim beyond the end of the list.
+// The persistent SNAC kernel.  With tickets, a CTA holds at most four claimed
+// items (the one it moves and the next three; three in lists with flags) and
+// processes them in claim order; every wait of an item refers to items with smaller indices, held by
+// running CTAs that process their own claims in increasing order, so the
+// smallest unfinished item can always proceed and the grid progresses.  A CTA
+// claims its next item only once its last claim returned an item of the list,
+// so every CTA makes exactly one claim beyond the end of the list.
 template <int DT, int OPS, bool BULK, bool ALIGN>
 __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kCtasPerSmAligned : kCtasPerSmSpliced)
     snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
@@ -1192,17 +1276,20 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     __shared__ __align__(16) Ref sref[ALIGN ? kMaxRefsPerItem : 1];
     __shared__ int s_ok;
     __shared__ unsigned long long s_epoch;
+    __shared__ unsigned s_claimed;
     extern __shared__ __align__(128) char dyn[];
     BulkRing bk{dyn + 128, reinterpret_cast<unsigned long long*>(dyn), stages, 0u,
-                reinterpret_cast<unsigned long long*>(dyn) + kBulkMaxStages, 0u};
+                reinterpret_cast<unsigned long long*>(dyn) + kBulkMaxStages, 0u, true};
     const int tid = (int)threadIdx.x;
     // With static claims the CTA's first item is blockIdx.x; when every item
     // has refs_per_item references in order, each thread loads its reference
     // of that item while thread 0 loads the header (one round trip less).
-    const bool early = !a.use_tickets && a.refs_per_item > 0 && blockIdx.x < a.nitems && tid < a.refs_per_item;
+    const bool early =
+        (!a.use_tickets || a.static_head) && a.refs_per_item > 0 && blockIdx.x < a.nitems && tid < a.refs_per_item;
     Ref r0{};
     if (early)
         r0 = a.refs[(size_t)blockIdx.x * (size_t)a.refs_per_item + (size_t)tid];
+    unsigned claimed = ~0u;  // thread 0: the claim of item 2, carried into the item loop
     if (tid == 0) {
         if (BULK) {
             for (int i = 0; i < stages; ++i)
@@ -1211,11 +1298,13 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
                 mbar_init(&bk.sbar[i], 1u);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
-        // The epoch of this launch (ticketed lists, which are the ones with
-        // flags): the last CTA out of the previous one advanced it.
-        s_epoch = a.use_tickets ? *reinterpret_cast<volatile const unsigned long long*>(a.st.epoch) : 0ull;
+        // The epoch of this launch (lists with flags, all ticketed): the last
+        // CTA out of the previous one advanced it.
+        s_epoch = a.use_tickets && !a.static_head ? *reinterpret_cast<volatile const unsigned long long*>(a.st.epoch)
+                                                  : 0ull;
         const unsigned i0 = claim(a, 0);
         const unsigned i1 = i0 < a.nitems ? claim(a, 1) : ~0u;
+        claimed = a.static_head && i1 < a.nitems ? claim(a, 2) : ~0u;  // read in the loop's first iteration
         // both header loads in flight before either is stored
         Item h0{}, h1{};
         if (i0 < a.nitems)
@@ -1233,11 +1322,17 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
     if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
         bad = put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
     // The loops' first barrier publishes sh[0] before item 0 moves.
-    if constexpr (ALIGN)
-        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch);
-    else
-        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch);
+    if constexpr (ALIGN) {
+        item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch, claimed);
+    } else {
+        if (tid == 0)
+            s_claimed = claimed;  // (once per launch: the claim's round trip ends here)
+        __syncthreads();
+        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch, &s_claimed);
+    }
 
+    if (BULK && tid == 0)
+        bulk_wait_all();  // the stores of items that did not drain have landed
     if (a.use_tickets && tid == 0) {
         __threadfence();
         if (atomicAdd(a.st.exited, 1u) == gridDim.x - 1) {
@@ -1246,7 +1341,8 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
             // larger than every tag of this one.
             *a.st.ticket = 0u;
             *a.st.exited = 0u;
-            *a.st.epoch = epoch + 1ull;
+            if (!a.static_head)
+                *a.st.epoch = epoch + 1ull;
             __threadfence();
         }
     }

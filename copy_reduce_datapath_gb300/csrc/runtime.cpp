@@ -41,6 +41,18 @@ constexpr int kGuidedDiv = 4;         // guided chunking: each item moves remain
 constexpr int kGuidedTailDiv = 16;    // ... down to a chunk of total / (kGuidedTailDiv x grid) bytes,
 constexpr uint64_t kGuidedTailMin = 64 << 10;   // kept within [kGuidedTailMin, kGuidedTailMax]
 constexpr uint64_t kGuidedTailMax = 256 << 10;
+// ... and, counted in bytes moved (read plus written), no larger than the
+// greater of these: so that an item of eight sources or destinations ends
+// the list with about 128 KiB moved, not 576 KiB (on GB300 the last items of
+// a ReduceScatterV of 128 MiB per rank took 29 us each on one CTA).
+constexpr uint64_t kGuidedTailMovedMin = 256 << 10;
+constexpr int kGuidedTailMovedDiv = 16;
+// Up to this many bytes moved, guided items start at remaining / (2 x grid)
+// instead of remaining / (kGuidedDiv x grid): fewer items, each paying the
+// fixed cost of a work item once (measured on GB300 at 64-128 MiB per rank:
+// AllGatherV 0.71 -> 0.75, ReduceScatterV 0.77 -> 0.84, AllToAllV 0.82 ->
+// 0.85 of the roofline; from 256 MiB per rank the finer start wins).
+constexpr uint64_t kGuidedCoarseMoved = 1536ull << 20;
 constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA: one item per CTA
 // ... and for plans of one-to-one transfers (the AllToAll shape; measured: the
 // AllToAllV of 16 MiB per rank, 431 KB per CTA, 63.3 us guided, 54.5 us with
@@ -770,6 +782,7 @@ enum class ChunkRule {
     kPerCta,  // small messages: each transfer's share of the grid, about one item per CTA
     kEqual,   // near-equal items, a few per CTA
     kGuided,  // guided self-scheduling: items shrink toward the end of the list
+    kGuidedRows,  // guided sizes per chunk row, every transfer cut alike (lists with flags)
 };
 
 // The codesign policy of one plan.
@@ -967,6 +980,8 @@ pl_status choose_policy(const PlanShape& sh, pl_op op, int R, const ResolvedPoli
     pp.rule = ChunkRule::kFixed;
     if (!pp.ticketed && pol.chunk_bytes == 0)
         choose_auto_rule(sh, op, pol, pp);
+    else if (pp.ticketed && !pp.staged && pol.chunk_bytes == 0)
+        pp.rule = ChunkRule::kGuidedRows;
     return PL_OK;
 }
 
@@ -993,13 +1008,15 @@ void cut_guided(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
     }
     const uint64_t tail_bytes =
         std::min(std::max(sh.total_bytes / (grid * kGuidedTailDiv), kGuidedTailMin), kGuidedTailMax);
-    const uint64_t min_elems = round_grain(tail_bytes / S);
+    const uint64_t tail_moved = std::max(kGuidedTailMovedMin, sh.moved / (grid * kGuidedTailMovedDiv));
+    const uint64_t div = sh.moved <= kGuidedCoarseMoved ? 2 : kGuidedDiv;
     const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
     // transfers take turns
     for (size_t k = 0; rem_moved > 0; k = (k + 1) % sh.ts.size()) {
         if (rem[k] == 0)
             continue;
-        uint64_t target = rem_moved / (grid * kGuidedDiv) / w[k];
+        const uint64_t min_elems = std::min(round_grain(tail_bytes / S), round_grain(tail_moved / w[k]));
+        uint64_t target = rem_moved / (grid * div) / w[k];
         target = std::min(std::max(round_grain(target), min_elems), max_elems);
         const Chunk ch = next_chunk(sh.ts[k], cur[k], target, E);
         const uint64_t got = ch.nrows * ch.ncols;
@@ -1010,12 +1027,56 @@ void cut_guided(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
     }
 }
 
+// kGuidedRows (the zero-staging composed AllReduce): chunk row c of every
+// transfer has one size, the guided size of the row (the bytes all transfers
+// still have to move / (kGuidedDiv x grid), within the guided tail and the
+// chunk cap), so that rows keep their meaning for the lag between a row's
+// producers and its consumers while the last rows are small: the grid ends
+// within a small item of itself instead of a large one.  (Measured on GB300
+// with equal chunks of total / (4 x grid): an AllReduce of 1 GiB per rank
+// had its median CTA done 10% before its last.)
+void cut_guided_rows(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
+{
+    const uint64_t S = sh.S, E = sh.E, grid = (uint64_t)pp.full_grid;
+    auto round_grain = [&](uint64_t elems) { return std::max(pp.grain, elems / pp.grain * pp.grain); };
+    std::vector<Cursor> cur(sh.ts.size());
+    std::vector<uint64_t> rem(sh.ts.size()), w(sh.ts.size());
+    uint64_t rem_moved = 0;
+    for (size_t i = 0; i < sh.ts.size(); ++i) {
+        rem[i] = sh.ts[i].count;
+        w[i] = S * (sh.ts[i].srcs.size() + sh.ts[i].dsts.size());
+        rem_moved += rem[i] * w[i];
+    }
+    // The smallest rows: total / (kGuidedTailDiv x grid), from kMinChunkBytes (a
+    // small message still gets several items per CTA) to kGuidedTailMax.
+    const uint64_t tail_bytes =
+        std::min(std::max(sh.total_bytes / (grid * kGuidedTailDiv), kMinChunkBytes), kGuidedTailMax);
+    const uint64_t min_elems = round_grain(tail_bytes / S);
+    const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
+    while (rem_moved > 0) {
+        const uint64_t row_moved = rem_moved;
+        for (size_t i = 0; i < sh.ts.size(); ++i) {
+            if (rem[i] == 0)
+                continue;
+            uint64_t target = row_moved / (grid * kGuidedDiv) / w[i];
+            target = std::min(std::max(round_grain(target), min_elems), max_elems);
+            const Chunk ch = next_chunk(sh.ts[i], cur[i], target, E);
+            const uint64_t got = ch.nrows * ch.ncols;
+            cu.chunks[i].push_back(ch);
+            rem[i] -= got;
+            rem_moved -= got * w[i];
+        }
+    }
+}
+
 Cuts cut_chunks(const PlanShape& sh, const PlanPolicy& pp)
 {
     Cuts cu;
     cu.chunks.resize(sh.ts.size());
     if (pp.rule == ChunkRule::kGuided) {
         cut_guided(sh, pp, cu);
+    } else if (pp.rule == ChunkRule::kGuidedRows) {
+        cut_guided_rows(sh, pp, cu);
     } else {
         for (size_t i = 0; i < sh.ts.size(); ++i) {
             if (pp.rule == ChunkRule::kFixed) {
@@ -2028,6 +2089,7 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in, const pl_layout
     a.all_aligned = dp->hp.all_aligned && !dp->hp.flagged_reduction;
     a.refs_per_item = dp->hp.refs_per_item;
     a.no_spread = in_place && (dp->hp.ops & kOpsReduce) ? 1 : 0;
+    a.static_head = ps.uses_tickets && ps.syncs == 0 ? 1 : 0;
     a.timeout_ns = rp.timeout_ns;
     a.drop_notify = rp.drop_notify;
     a.st = ctx->st;

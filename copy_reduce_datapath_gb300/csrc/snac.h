@@ -105,6 +105,8 @@ struct LaunchArgs {
     int32_t all_aligned;         // every reference's offset (and row stride) is a multiple of 16 bytes
     int32_t refs_per_item;       // n > 0: item i's references are refs[i * n .. i * n + n); 0: read the header
     int32_t no_spread;           // 1: every vector is read and written by one thread (a reduction in place)
+    int32_t static_head;         // 1 (ticketed lists without flags): each CTA's first two items are static,
+                                 // blockIdx.x and blockIdx.x + grid; the ticket hands out the rest from 2 x grid
     unsigned long long timeout_ns;
     long long drop_notify;       // item index whose notifies are skipped, or -1
     DeviceState st;

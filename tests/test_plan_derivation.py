@@ -258,8 +258,10 @@ def test_one_byte_chunks_and_alignment():
 def test_automatic_chunking_covers_every_element(kind, scale):
     """Automatic chunks of plans whose items never wait (zero-staging), on a
     4-SM grid: about one item per CTA for small messages (scale 1: under
-    256 KiB per CTA), guided sizes that shrink along the list for larger ones
-    (scale 20), claimed in order once there are more items than CTAs.
+    256 KiB per CTA); for larger ones (scale 20) one large item per CTA and a
+    few small ones after it (the V forms), or guided sizes that shrink along
+    the list (strided rows), claimed in order once there are more items than
+    CTAs.
     Executed by the emulator, the result equals the oracle.  (The vector
     datapath: the persistent kernel's chunk rule, not the inline form's.)"""
     R, dtype = 8, "bf16"
