@@ -738,11 +738,11 @@ __device__ void bulk_shift_copy(BulkRing& bk, const ItemShared& sh, unsigned lon
 // The kernels for plans not proven aligned move every vector body through
 // here, aligned or not: one body instead of three keeps them within the
 // register budget.
-template <int DT, bool MAXOP, bool SUM, bool WIDE>
+template <int DT, bool MAXOP, bool SUM, bool WIDE, int CU = 8>
 __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                              size_t body, unsigned nv, int q, int tid, int nthr)
 {
-    constexpr int U = SUM ? (WIDE ? 1 : 2) : 8;  // warp steps in flight per thread
+    constexpr int U = SUM ? (WIDE ? 1 : 2) : CU;  // warp steps in flight per thread (a copy: CU)
     constexpr int G = SUM ? 8 / U : 1;           // sources in flight per step
     const int lane = tid & 31;
     const unsigned warp = (unsigned)tid >> 5;
@@ -982,7 +982,8 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
             // a source misaligned against aligned destinations (q0 != 0 here)
             bulk_shift_copy(bk, sh, mask, row, body, SRC_ROW(sh, 0, row) + body - q0, q0, nv, tid, nthr, a);
         } else {
-            shifted_body<DT, false, false, false>(sh, 1, mask, row, body, nv, q0, tid, nthr);
+            // the copy-only kernels run half the threads with twice the vectors in flight
+            shifted_body<DT, false, false, false, OPS == kOpsCopy ? 16 : 8>(sh, 1, mask, row, body, nv, q0, tid, nthr);
         }
     } else if constexpr (REDUCE) {
         constexpr bool WIDE = (OPS & kOpsWide) != 0;
@@ -1201,8 +1202,6 @@ __device__ __forceinline__ void item_loop_async(const LaunchArgs& a, ItemShared*
 // its load (measured on GB300: 1.5-2 us per item when thread 0, which drives
 // the bulk ring, issued them before the barrier).  After the barrier that
 // wait overlaps the move's own first loads.
-constexpr int kPrefetchThread = 32;
-
 template <int DT, int OPS, bool BULK>
 __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* sh, Slot* slot, int* s_ok,
                                                BulkRing& bk, int tid, bool bad, unsigned long long epoch,
@@ -1260,6 +1259,89 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
     }
 }
 
+// Work-item loop of the copy-only spliced kernels (256 threads): nothing is
+// held in registers across the move; the references of item k+1 and the
+// header of item k+2 come into shared memory by asynchronous copies, and the
+// headers stay in a ring of three slots that the loop reads in place.  The
+// copies and the claim are issued by threads kPrefetchThread onwards after
+// the barrier that starts the move, where any wait on them overlaps the
+// move's own first loads; thread 0, which drives the bulk ring, starts at
+// once.  (Measured on GB300: AllToAllV 1 GiB 0.95 -> 0.98 of the roofline
+// against the register form below; the reductions' kernels lost with this
+// form, 0.99 -> 0.96 on the ReduceScatterV at 1 GiB.)
+template <int DT, int OPS, bool BULK>
+__device__ __forceinline__ void item_loop_copy(const LaunchArgs& a, ItemShared* sh, Slot* slot, Ref* sref,
+                                                  int* s_ok, BulkRing& bk, int tid, bool bad,
+                                                  unsigned long long epoch, const unsigned* s_claimed)
+{
+    const int rt = tid - kPrefetchThread;  // the reference of the next item this thread copies
+    // `claimed` (thread kPrefetchThread, lists without flags): the index
+    // claimed for item k+2, ~0u once a claim has returned the end of the list.
+    unsigned claimed = tid == kPrefetchThread ? *s_claimed : ~0u;
+    for (unsigned k = 0;; ++k) {
+        const int cur = (int)(k % 3u), nxt = (int)((k + 1u) % 3u), nn = (int)((k + 2u) % 3u);
+        const int scur = (int)(k & 1u), snxt = scur ^ 1;
+        const unsigned index = slot[cur].index;
+        if (index >= a.nitems)
+            break;
+        if (tid < 32) {
+            const bool ok = slot[cur].item.nwait ? run_waits(a, slot[cur].item, tid, epoch) : true;
+            if (tid == 0)
+                *s_ok = ok ? 1 : 0;
+        }
+        // `bad`: this thread's reference of item k is misaligned (put_ref)
+        const bool proven = !__syncthreads_or(bad);
+        const bool ok = *s_ok != 0;  // read by every thread before the next write (after the barrier below)
+        const bool has_next = slot[nxt].index < a.nitems;
+        if (has_next) {
+            // slot[nn] last held item k-1, whose posts ended before the barrier above
+            const Item& nit = slot[nxt].item;
+            if (rt >= 0 && rt < nit.nsrc + nit.ndst) {
+                const char* g = reinterpret_cast<const char*>(a.refs + nit.ref + rt);
+                char* d = reinterpret_cast<char*>(&sref[rt]);
+                cp_async8(d, g);
+                cp_async8(d + 8, g + 8);
+                cp_async8(d + 16, g + 16);
+            }
+            if (tid == kPrefetchThread) {
+                const unsigned i2 = a.static_head ? claimed : claim(a, k + 2);
+                slot[nn].index = i2;
+                claimed = ~0u;
+                if (i2 < a.nitems) {
+                    const char* g = reinterpret_cast<const char*>(a.items + i2);
+                    char* d = reinterpret_cast<char*>(&slot[nn].item);
+                    cp_async16(d, g);
+                    cp_async16(d + 16, g + 16);
+                    if (a.static_head)
+                        claimed = claim(a, k + 3);  // read in the next iteration
+                }
+            }
+        } else if (tid == kPrefetchThread) {
+            slot[nn].index = ~0u;
+        }
+        cp_async_commit();
+        bk.drain = slot[cur].item.npost != 0;
+        if (ok) {
+            const Item& it = slot[cur].item;
+            move_item<DT, OPS, BULK, false>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
+        }
+        cp_async_wait_all();
+        bad = false;
+        if (has_next) {
+            // this thread's own copy of the reference; sh[snxt] served item k-1
+            const Item& nit = slot[nxt].item;
+            if (rt >= 0 && rt < nit.nsrc + nit.ndst)
+                bad = put_ref<DT>(a, nit, sref[rt], sh[snxt], rt);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            if (ok && slot[cur].item.npost)
+                run_posts(a, slot[cur].item, index, tid, epoch);
+            __syncwarp();
+        }
+    }
+}
+
 // The persistent SNAC kernel.  With tickets, a CTA holds at most four claimed
 // items (the one it moves and the next three; three in lists with flags) and
 // processes them in claim order; every wait of an item refers to items with smaller indices, held by
@@ -1268,12 +1350,13 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
 // claims its next item only once its last claim returned an item of the list,
 // so every CTA makes exactly one claim beyond the end of the list.
 template <int DT, int OPS, bool BULK, bool ALIGN>
-__global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kCtasPerSmAligned : kCtasPerSmSpliced)
+__global__ void __launch_bounds__(ALIGN ? kThreads : OPS == kOpsCopy ? kThreadsSplicedCopy : kThreadsSpliced,
+                                  ALIGN ? kCtasPerSmAligned : kCtasPerSmSpliced)
     snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
 {
     __shared__ ItemShared sh[2];
     __shared__ Slot slot[3];
-    __shared__ __align__(16) Ref sref[ALIGN ? kMaxRefsPerItem : 1];
+    __shared__ __align__(16) Ref sref[kMaxRefsPerItem];
     __shared__ int s_ok;
     __shared__ unsigned long long s_epoch;
     __shared__ unsigned s_claimed;
@@ -1328,7 +1411,10 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : kThreadsSpliced, ALIGN ? kC
         if (tid == 0)
             s_claimed = claimed;  // (once per launch: the claim's round trip ends here)
         __syncthreads();
-        item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch, &s_claimed);
+        if constexpr (OPS == kOpsCopy)
+            item_loop_copy<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch, &s_claimed);
+        else
+            item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch, &s_claimed);
     }
 
     if (BULK && tid == 0)
@@ -1371,7 +1457,8 @@ cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_
             configured.fetch_or(bit, std::memory_order_acq_rel);
         }
     }
-    snac_kernel<DT, OPS, BULK, ALIGN><<<ctas, ALIGN ? kThreads : kThreadsSpliced, dyn, stream>>>(args, stages);
+    constexpr int threads = ALIGN ? kThreads : OPS == kOpsCopy ? kThreadsSplicedCopy : kThreadsSpliced;
+    snac_kernel<DT, OPS, BULK, ALIGN><<<ctas, threads, dyn, stream>>>(args, stages);
     return cudaGetLastError();
 }
 

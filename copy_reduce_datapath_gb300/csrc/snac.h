@@ -14,7 +14,16 @@ constexpr int kMaxRanks = 64;
 constexpr int kMaxRefsPerItem = 2 * kMaxRanks + 1;  // R sources + R destinations + one slot
 constexpr int kThreads = 512;                        // threads per CTA of the kernels for aligned plans
 constexpr int kThreadsSpliced = 512;                 // threads per CTA of the kernels for other plans
-static_assert(kThreads >= kMaxRefsPerItem && kThreadsSpliced >= kMaxRefsPerItem,
+// ... and of those among them whose lists only copy: half the threads, each
+// with twice the vectors in flight (16), and 128 registers, so nothing
+// spills; the bulk ring's realignment and its barrier per piece also go
+// faster with fewer threads.  Measured on GB300: AllGatherV 64 MiB 0.80 ->
+// 0.84 of the roofline, AllToAllV 1 GiB 0.95 -> 0.98; the reductions lose
+// with fewer threads (ReduceScatterV 128 MiB 0.84 -> 0.78), so they keep 512.
+constexpr int kThreadsSplicedCopy = 256;
+constexpr int kPrefetchThread = 32;  // the spliced kernels' first thread that prefetches the next item
+static_assert(kThreads >= kMaxRefsPerItem && kThreadsSpliced >= kPrefetchThread + kMaxRefsPerItem &&
+                  kThreadsSplicedCopy >= kPrefetchThread + kMaxRefsPerItem,
               "one thread per region reference of an item");
 constexpr int kBulkMaxStages = 8;
 // CTAs per SM the kernels are built for: those for plans proven 16-byte
