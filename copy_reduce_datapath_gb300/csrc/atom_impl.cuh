@@ -1259,17 +1259,19 @@ __device__ __forceinline__ void item_loop_regs(const LaunchArgs& a, ItemShared* 
     }
 }
 
-// Work-item loop of the copy-only spliced kernels (256 threads): nothing is
-// held in registers across the move; the references of item k+1 and the
+// Work-item loop of the copy-only kernels (the spliced ones at 256 threads,
+// the aligned ones at 512): nothing is held in registers across the move; the references of item k+1 and the
 // header of item k+2 come into shared memory by asynchronous copies, and the
 // headers stay in a ring of three slots that the loop reads in place.  The
 // copies and the claim are issued by threads kPrefetchThread onwards after
 // the barrier that starts the move, where any wait on them overlaps the
 // move's own first loads; thread 0, which drives the bulk ring, starts at
 // once.  (Measured on GB300: AllToAllV 1 GiB 0.95 -> 0.98 of the roofline
-// against the register form below; the reductions' kernels lost with this
-// form, 0.99 -> 0.96 on the ReduceScatterV at 1 GiB.)
-template <int DT, int OPS, bool BULK>
+// against the register form below, and the aligned AllGather and AllToAll
+// 1-2% faster than with the prefetch before the barrier; the reductions'
+// kernels lost with this form: ReduceScatterV 1 GiB 0.99 -> 0.96, the aligned
+// AllReduce at 128 MiB 0.95 -> 0.93.)
+template <int DT, int OPS, bool BULK, bool ALIGN>
 __device__ __forceinline__ void item_loop_copy(const LaunchArgs& a, ItemShared* sh, Slot* slot, Ref* sref,
                                                   int* s_ok, BulkRing& bk, int tid, bool bad,
                                                   unsigned long long epoch, const unsigned* s_claimed)
@@ -1323,7 +1325,7 @@ __device__ __forceinline__ void item_loop_copy(const LaunchArgs& a, ItemShared* 
         bk.drain = slot[cur].item.npost != 0;
         if (ok) {
             const Item& it = slot[cur].item;
-            move_item<DT, OPS, BULK, false>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
+            move_item<DT, OPS, BULK, ALIGN>(sh[scur], it.nsrc, it.ndst, it.rows, it.cols, bk, a, proven);
         }
         cp_async_wait_all();
         bad = false;
@@ -1405,14 +1407,14 @@ __global__ void __launch_bounds__(ALIGN ? kThreads : OPS == kOpsCopy ? kThreadsS
     if (slot[0].index < a.nitems && tid < slot[0].item.nsrc + slot[0].item.ndst)
         bad = put_ref<DT>(a, slot[0].item, early ? r0 : a.refs[slot[0].item.ref + tid], sh[0], tid);
     // The loops' first barrier publishes sh[0] before item 0 moves.
-    if constexpr (ALIGN) {
+    if constexpr (ALIGN && OPS != kOpsCopy) {
         item_loop_async<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch, claimed);
     } else {
         if (tid == 0)
             s_claimed = claimed;  // (once per launch: the claim's round trip ends here)
         __syncthreads();
         if constexpr (OPS == kOpsCopy)
-            item_loop_copy<DT, OPS, BULK>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch, &s_claimed);
+            item_loop_copy<DT, OPS, BULK, ALIGN>(a, sh, slot, sref, &s_ok, bk, tid, bad, epoch, &s_claimed);
         else
             item_loop_regs<DT, OPS, BULK>(a, sh, slot, &s_ok, bk, tid, bad, epoch, &s_claimed);
     }
