@@ -413,6 +413,17 @@ def plan_form(P, lin, lout, op, dtype, Rr, num_sms):
     return {P.PL_ATOM_INLINE: "inline", P.PL_ATOM_BULK: "bulk", P.PL_ATOM_VECTOR: "vector"}.get(st.datapath, "?")
 
 
+def plan_bytes(P, lin, lout, op, dtype, Rr, pol, num_sms, scratch):
+    """Device bytes one launch of the plan reads and writes (its own bytes:
+    staging and rereads included)."""
+    plan = P.pl_plan_create(lin, lout, op, dtype, Rr, pol, num_sms, scratch)
+    try:
+        st = P.pl_plan_get_stats(plan)
+    finally:
+        P.pl_plan_destroy(plan)
+    return int(st.bytes_read + st.bytes_written)
+
+
 def point(us, T, moved, peak, how, form=None):
     """One timed point: latency, algbw (T / time), algorithmic HBM bandwidth
     and its fraction of the copy peak."""
@@ -448,7 +459,14 @@ def time_configs(ctx, wl, stream, torch, peak):
         token groups) and the Ulysses sequence-to-head swap ([16384, 32, 128]
         bf16 per rank);
       - the copy-engine AllGather (one memcpy per source and destination pair,
-        no kernel) beside the library's AllGather at 64 MiB and 1 GiB.
+        no kernel) beside the library's AllGather at 64 MiB and 1 GiB;
+      - the AllReduce of the benchmark (R = 8, bf16) in its three forms at
+        64 MiB, 128 MiB and 1 GiB: fused, composed at vector grain and composed
+        per chunk with a Notify (Figure 6), each against the fused form's
+        algorithmic bytes (16T) and with the plan's own bytes;
+      - the staged SNAC path (Stage, Notify, Consume through a scratch ring) at
+        128 MiB and 1 GiB: ReduceScatter and the fused and composed AllReduce,
+        each against its plan's own bytes (staging included).
     The Zipf V forms are in the sweep."""
     import synth
     P = wl.P
@@ -529,6 +547,53 @@ def time_configs(ctx, wl, stream, torch, peak):
         ce.append({"T": T, "memcpy_per_pair": point(us_m, T, moved, peak, how_m),
                    "kernel": point(us_k, T, moved, peak, how_k, wl.sweep_form("allgather", T, sms))})
     out["copy_engine_allgather"] = ce
+
+    # the AllReduce forms on the benchmark's AllReduce buffers
+    forms = {"fused": P.PL_AR_FUSED, "composed": P.PL_AR_COMPOSED, "notified": P.PL_AR_NOTIFIED}
+    arf = []
+    for T in (64 << 20, 128 << 20, wl.T):
+        n = T // 2
+        L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
+        pi, po = P.ptrs(wl.ar_in), P.ptrs(wl.ar_out)
+        for name, form in forms.items():
+            pol = P.pl_policy_default(allreduce_form=form)
+            us, how = time_call(lambda: P.pl_allreduce(ctx, "bf16", R, n, pi, po, pol, s), T, stream, torch)
+            own = plan_bytes(P, L, L, "sum", "bf16", R, pol, sms, 0)
+            arf.append({"T": T, "form": name, "plan_bytes": own, "own_frac": round(own / (us * 1e-6) / 1e9 / peak, 4),
+                        **point(us, T, 2 * R * T, peak, how)})
+        P.pl_layout_destroy(L)
+    out["allreduce_forms"] = arf
+
+    # the staged path, with a context that owns a scratch ring
+    scratch = GiB
+    sctx = P.pl_ctx_create(dev.index or 0, scratch)
+    staged = []
+    try:
+        for T in (128 << 20, wl.T):
+            n = T // 2
+            lens = synth.equal_lengths(n, R)
+            L = P.pl_layout_partitioned(R, lens)
+            lo = P.pl_layout_rank_owned(R, lens)
+            pi, po = P.ptrs(wl.ar_in), P.ptrs(wl.ar_out)
+            cases = (("reducescatter", lo, P.pl_policy_default(path=P.PL_PATH_STAGED), (R + 1) * T),
+                     ("allreduce_fused", L, P.pl_policy_default(path=P.PL_PATH_STAGED), 2 * R * T),
+                     ("allreduce_composed", L, P.pl_policy_default(path=P.PL_PATH_STAGED,
+                                                                   allreduce_form=P.PL_AR_COMPOSED), 2 * R * T))
+            for name, lout, pol, alg in cases:
+                cout = lens if lout is lo else [n] * R
+                call = lambda: P.pl_collective(sctx, L, lout, "sum", "bf16", R, pi, [n] * R, po, cout, pol, s)  # noqa: E731
+                us, how = time_call(call, T, stream, torch)
+                own = plan_bytes(P, L, lout, "sum", "bf16", R, pol, sms, scratch)
+                staged.append({"T": T, "collective": name, "plan_bytes": own,
+                               "algorithmic_frac": round(alg / (us * 1e-6) / 1e9 / peak, 4),
+                               **point(us, T, own, peak, how)})
+            P.pl_layout_destroy(L)
+            P.pl_layout_destroy(lo)
+        torch.cuda.synchronize()
+        assert P.pl_ctx_status(sctx, s) == P.PL_OK
+    finally:
+        P.pl_ctx_destroy(sctx)
+    out["staged"] = staged
     out["note"] = ("points up to 64 MiB replay a CUDA graph on the same buffers back to back, so below the L2 size "
                    "(129 MB of working set) they measure latency and L2 bandwidth, and frac_of_peak can exceed 1; "
                    "from 128 MiB up, events around back-to-back calls on buffers larger than L2")

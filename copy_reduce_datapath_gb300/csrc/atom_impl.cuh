@@ -553,6 +553,87 @@ __device__ __forceinline__ void sum_mixed(const ItemShared& sh, int nsrc, unsign
     }
 }
 
+// Figure 6 at the grain of one vector (kCompose items, aligned plans): the
+// rank-ordered reduction of nv vectors is stored to destination 0, the
+// partition's owner; the same thread then reads each reduced vector back from
+// the owner's output and writes it to the other destinations in `mask`.  A
+// thread's load of an address it stored returns what it stored (program
+// order), so no flag is needed between the reduce and the gather, and the
+// reread is served by L2 (measured on GB300: DRAM reads of an AllReduce 8T,
+// as with the fused form).  The reread of one step is issued with the source
+// loads of the next, so its latency hides behind theirs.  U vectors x G
+// sources in flight per thread, as in sum_aligned.
+template <int DT, bool MAXOP, int U>
+__device__ __forceinline__ void sum_compose(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
+                                            size_t body, unsigned nv, int tid, int nthr)
+{
+    constexpr int G = 8 / U;
+    const unsigned step = (unsigned)nthr * U;
+    char* const own = DST_ROW(sh, 0, row) + body;
+    const unsigned long long rest = mask & ~1ull;
+    unsigned prev = ~0u;  // the first vector of this thread's previous step
+    for (unsigned v0 = tid;; v0 += step) {
+        const bool cur = v0 < nv;
+        uint4 back[U];
+        if (prev != ~0u) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = prev + u * nthr;
+                if (v < nv)
+                    back[u] = ld16(own + (size_t)v * 16);
+            }
+        }
+        if (cur) {
+            Acc<DT, MAXOP> acc[U];
+            for (int s0 = 0; s0 < nsrc; s0 += G) {
+                uint4 x[U][G];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const unsigned v = v0 + u * nthr;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        if (s0 + g < nsrc && v < nv)
+                            x[u][g] = ld16(SRC_ROW(sh, s0 + g, row) + body + (size_t)v * 16);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (s0 + g < nsrc) {
+                            if (s0 + g == 0)
+                                acc[u].set(x[u][g]);
+                            else
+                                acc[u].add(x[u][g]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = v0 + u * nthr;
+                if (v < nv)
+                    st16(own + (size_t)v * 16, acc[u].pack());
+            }
+        }
+        if (prev != ~0u) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const unsigned v = prev + u * nthr;
+                if (v < nv) {
+#pragma unroll 1
+                    for (unsigned long long m = rest; m; m &= m - 1) {
+                        const int d = __ffsll((long long)m) - 1;
+                        st16(DST_ROW(sh, d, row) + body + (size_t)v * 16, back[u]);
+                    }
+                }
+            }
+        }
+        if (!cur)
+            break;
+        prev = v0;
+    }
+}
+
 template <int DT, bool MAXOP, bool WIDE>
 __device__ __forceinline__ void sum_body(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                          size_t body, unsigned nv, int tid, int nthr)
@@ -823,8 +904,9 @@ __device__ __forceinline__ void shifted_body(const ItemShared& sh, int nsrc, uns
 // A multi-row block whose rows are whole 16-byte vectors at 16-byte aligned
 // addresses in every source and destination: one flat index over
 // rows x vectors-per-row spread over the whole CTA (no per-row heads, tails
-// or realignment).
-template <int DT, bool MAXOP, bool SUM, int U>
+// or realignment).  COMP (a kCompose item): each reduced vector is stored to
+// destination 0, read back from there and written to the others.
+template <int DT, bool MAXOP, bool SUM, int U, bool COMP = false>
 __device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int ndst, unsigned rows, unsigned vpr,
                                             int tid, int nthr)
 {
@@ -871,9 +953,16 @@ __device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int 
                     }
                 }
             }
-            const uint4 out = acc.pack();
+            uint4 out = acc.pack();
+            int d = 0;
+            if constexpr (COMP) {
+                char* const own = DST_ROW(sh, 0, rr) + (size_t)cc * 16;
+                st16(own, out);
+                out = ld16(own);
+                d = 1;
+            }
 #pragma unroll 1
-            for (int d = 0; d < ndst; ++d)
+            for (; d < ndst; ++d)
                 st16(DST_ROW(sh, d, rr) + (size_t)cc * 16, out);
         }
     }
@@ -883,7 +972,10 @@ __device__ __forceinline__ void flat2d_body(const ItemShared& sh, int nsrc, int 
 // Destinations in `mask` share the same address mod 16 (`dcls`); their
 // stores are 16-byte aligned after a head of at most 16/S - 1 elements, and
 // the rest up to the last whole vector goes through the vector bodies.
-template <int DT, int OPS, bool BULK, bool ALIGN>
+// COMP (kCompose items, aligned kernels): `mask` holds every destination,
+// destination 0 first; each reduced value is stored to destination 0 and
+// written to the others from there.
+template <int DT, int OPS, bool BULK, bool ALIGN, bool COMP = false>
 __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned long long mask, unsigned row,
                                         unsigned n, unsigned dcls, int tid, int nthr, BulkRing& bk,
                                         const LaunchArgs& a, bool proven)
@@ -901,10 +993,13 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
     if (ALIGN && !proven) {
         // Kernels built for plans the host proved 16-byte aligned have no
         // realigning bodies; should a segment still be misaligned, it is moved
-        // element by element below (correct, slower).
+        // element by element below (correct, slower).  A composed item's
+        // destinations then differ in alignment too: all of it element-wise.
         for (int s = 0; s < nsrc; ++s)
             if (((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + (size_t)head * S) & 15u) != 0)
                 nv = 0;
+        if (COMP)
+            nv = 0;
     }
     const unsigned tail0 = head + nv * E;
     const unsigned ntail = n - tail0;
@@ -935,8 +1030,15 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         } else {
             v = EL::load(SRC_ROW(sh, 0, row) + (size_t)i * S);
         }
+        unsigned long long rest = mask;
+        if constexpr (COMP) {
+            char* const own = DST_ROW(sh, 0, row) + (size_t)i * S;
+            EL::store(own, v);
+            v = EL::load(own);
+            rest &= ~1ull;
+        }
 #pragma unroll 1
-        for (unsigned long long m = mask; m; m &= m - 1) {
+        for (unsigned long long m = rest; m; m &= m - 1) {
             const int d = __ffsll((long long)m) - 1;
             EL::store(DST_ROW(sh, d, row) + (size_t)i * S, v);
         }
@@ -955,7 +1057,7 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
             uniform &= (int)((reinterpret_cast<uintptr_t>(SRC_ROW(sh, s, row)) + body) & 15u) == q0;
     }
     const bool aligned = uniform && q0 == 0;
-    if (ALIGN && proven && !a.no_spread) {
+    if (ALIGN && proven && !a.no_spread && !COMP) {
         // A small item: one thread per (vector, destination), so the item's
         // stores issue at once instead of one destination after another (the
         // bodies below take any thread count).  Proven items come with the
@@ -987,7 +1089,9 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
         }
     } else if constexpr (REDUCE) {
         constexpr bool WIDE = (OPS & kOpsWide) != 0;
-        if (ALIGN)
+        if constexpr (ALIGN && COMP)
+            sum_compose<DT, MAXOP, WIDE ? 1 : 2>(sh, nsrc, mask, row, body, nv, tid, nthr);
+        else if (ALIGN)
             sum_body<DT, MAXOP, WIDE>(sh, nsrc, mask, row, body, nv, tid, nthr);
         else if (uniform)
             shifted_body<DT, MAXOP, true, WIDE>(sh, nsrc, mask, row, body, nv, q0, tid, nthr);
@@ -1002,8 +1106,10 @@ __device__ __forceinline__ void segment(const ItemShared& sh, int nsrc, unsigned
 // reference's row 0 and row stride are 16-byte aligned (checked per reference,
 // in parallel, when the references were loaded), so all destinations form one
 // group and no source needs realigning; the per-reference checks are skipped.
-template <int DT, int OPS, bool BULK, bool ALIGN>
-__device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
+// COMP: a kCompose item in an aligned kernel (all destinations one group,
+// destination 0 written first and read back for the others).
+template <int DT, int OPS, bool BULK, bool ALIGN, bool COMP>
+__device__ __forceinline__ void move_rows(const ItemShared& sh, int nsrc, int ndst, unsigned rows,
                                           unsigned long long cols, BulkRing& bk, const LaunchArgs& a, bool proven)
 {
     constexpr int S = Elem<DT>::S;
@@ -1023,7 +1129,8 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
                 flat2d_body<DT, false, false, kCopyUnroll>(sh, 1, ndst, rows, vpr, (int)threadIdx.x,
                                                           (int)blockDim.x);
             else if constexpr (REDUCE)
-                flat2d_body<DT, MAXOP, true, 1>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x, (int)blockDim.x);
+                flat2d_body<DT, MAXOP, true, 1, COMP>(sh, nsrc, ndst, rows, vpr, (int)threadIdx.x,
+                                                      (int)blockDim.x);
             return;
         }
     }
@@ -1038,7 +1145,7 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
         while (todo) {
             unsigned cls = 0;
             unsigned long long group = todo;
-            if (!proven) {
+            if (!proven && !COMP) {
                 const int d0 = __ffsll((long long)todo) - 1;
                 cls = (unsigned)(reinterpret_cast<uintptr_t>(DST_ROW(sh, d0, r)) & 15u);
                 group = 0;
@@ -1049,8 +1156,53 @@ __device__ __forceinline__ void move_item(const ItemShared& sh, int nsrc, int nd
                 }
             }
             todo &= ~group;
-            segment<DT, OPS, BULK, ALIGN>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a, proven);
+            segment<DT, OPS, BULK, ALIGN, COMP>(sh, nsrc, group, r, (unsigned)cols, cls, tid, nthr, bk, a, proven);
         }
+    }
+}
+
+// Moves one work item (all threads of the CTA).  A kCompose item (Figure 6)
+// runs at the grain of one vector in the aligned kernels (move_rows, COMP).
+// The kernels for other plans compose it per item instead: the reduction
+// into destination 0, a CTA barrier, which makes those stores visible to
+// every thread of the CTA, and then a move whose one source is destination 0
+// and whose destinations are the others (the item's shared image is
+// rewritten for it: this item's last use of it).
+template <int DT, int OPS, bool BULK, bool ALIGN>
+__device__ __forceinline__ void move_item(ItemShared& sh, int nsrc, int ndst, unsigned rows,
+                                          unsigned long long cols, BulkRing& bk, const LaunchArgs& a, bool proven)
+{
+    constexpr bool COMPOSE = (OPS & kOpsCompose) != 0;
+    if constexpr (COMPOSE && !ALIGN) {
+        // one inlined move for both steps (the register budget of these kernels)
+        const bool two = nsrc > 1 && ndst > 1;
+        for (int step = 0;; ++step) {
+            move_rows<DT, OPS, BULK, ALIGN, false>(sh, step ? 1 : nsrc, two ? (step ? ndst - 1 : 1) : ndst, rows,
+                                                   cols, bk, a, proven);
+            if (!two || step)
+                return;
+            const int t = (int)threadIdx.x;
+            char* d = nullptr;
+            unsigned long long ds = 0;
+            if (t + 1 < ndst) {
+                d = sh.dst[t + 1];
+                ds = sh.dstride[t + 1];
+            }
+            char* const own = sh.dst[0];
+            const unsigned long long os = sh.dstride[0];
+            __syncthreads();
+            if (t + 1 < ndst) {
+                sh.dst[t] = d;
+                sh.dstride[t] = ds;
+            }
+            if (t == 0) {
+                sh.src[0] = own;
+                sh.sstride[0] = os;
+            }
+            __syncthreads();
+        }
+    } else {
+        move_rows<DT, OPS, BULK, ALIGN, COMPOSE && ALIGN>(sh, nsrc, ndst, rows, cols, bk, a, proven);
     }
 }
 
@@ -1466,7 +1618,8 @@ cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_
 
 // One instantiation per mix of moves a work list can hold: copies only,
 // reductions only (wide for 2-byte sums of 8+ sources), or both, each with
-// the sum or the maximum.  The bulk ring serves copy items only.
+// the sum or the maximum; and reductions composed as in Figure 6 (kCompose
+// items, every transfer reduced).  The bulk ring serves copy items only.
 template <int DT, bool BULK, bool ALIGN>
 cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_t stream)
 {
@@ -1489,6 +1642,14 @@ cudaError_t launch_ops(const LaunchArgs& args, int ctas, int stages, cudaStream_
         case kOpsReduce | kOpsWide:
             if constexpr (Elem<DT>::S == 2)
                 return launch_one<DT, kOpsReduce | kOpsWide, false, ALIGN>(args, ctas, stages, stream);
+            return cudaErrorInvalidValue;
+        case kOpsReduce | kOpsCompose:
+            return launch_one<DT, kOpsReduce | kOpsCompose, false, ALIGN>(args, ctas, stages, stream);
+        case kOpsReduce | kOpsMax | kOpsCompose:
+            return launch_one<DT, kOpsReduce | kOpsMax | kOpsCompose, false, ALIGN>(args, ctas, stages, stream);
+        case kOpsReduce | kOpsWide | kOpsCompose:
+            if constexpr (Elem<DT>::S == 2)
+                return launch_one<DT, kOpsReduce | kOpsWide | kOpsCompose, false, ALIGN>(args, ctas, stages, stream);
             return cudaErrorInvalidValue;
         default:
             return cudaErrorInvalidValue;

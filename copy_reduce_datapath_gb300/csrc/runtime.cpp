@@ -381,7 +381,7 @@ struct Chunk {
 
 struct ResolvedPolicy {
     int path;       // PL_PATH_ZS / PL_PATH_STAGED
-    int ar_form;    // PL_AR_FUSED / PL_AR_COMPOSED
+    int ar_form;    // PL_AR_FUSED / PL_AR_COMPOSED / PL_AR_NOTIFIED
     int datapath;   // PL_ATOM_VECTOR / PL_ATOM_BULK / PL_ATOM_INLINE
     bool datapath_auto;
     bool stages_auto;
@@ -400,7 +400,7 @@ pl_status resolve_policy(const pl_policy* p, ResolvedPolicy& rp)
         p = &d;
     if (p->path < PL_PATH_AUTO || p->path > PL_PATH_STAGED)
         return PL_ERR_INVALID;
-    if (p->allreduce_form < PL_AR_AUTO || p->allreduce_form > PL_AR_COMPOSED)
+    if (p->allreduce_form < PL_AR_AUTO || p->allreduce_form > PL_AR_NOTIFIED)
         return PL_ERR_INVALID;
     if (p->datapath < PL_ATOM_AUTO || p->datapath > PL_ATOM_INLINE)
         return PL_ERR_INVALID;
@@ -791,6 +791,7 @@ struct PlanPolicy {
     bool ticketed = false;           // items wait on flags: claimed in index order
     bool flagged_reduction = false;  // a list with flags that reduces: the two-CTA kernels
     bool composed = false;           // reductions with several destinations: the Figure 6 form
+    bool vector_compose = false;     // ... zero-staging, at the grain of one vector (kCompose items, no flags)
     bool bulk = false;               // copy items of one-row regions go through the bulk ring
     int full_grid = 1;               // persistent grid for the plan's kernel class
     ChunkRule rule = ChunkRule::kFixed;
@@ -877,7 +878,7 @@ void choose_auto_rule(const PlanShape& sh, pl_op op, const ResolvedPolicy& pol, 
 {
     const uint64_t S = sh.S;
     const uint64_t grid = (uint64_t)pp.full_grid;
-    const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && sh.moved > 0 &&
+    const bool want_inline = pol.path == PL_PATH_ZS && pol.ctas == 0 && sh.moved > 0 && !pp.vector_compose &&
                              (pol.datapath == PL_ATOM_INLINE ||
                               (pol.datapath_auto && ((sh.rs_shape && sh.regions_aligned) || sh.moved <= kInlineAutoMoved)));
     if (want_inline && inline_targets(sh, op, pp.grain, pp.target)) {
@@ -925,8 +926,12 @@ pl_status choose_policy(const PlanShape& sh, pl_op op, int R, const ResolvedPoli
               (pol.datapath == PL_ATOM_BULK ||
                (sh.moved >= kBulkAutoBytes && (sh.all_aligned_regions || sh.wr >= 2 * sh.rd)));
     pp.staged = pol.path == PL_PATH_STAGED;
-    pp.composed = pol.ar_form == PL_AR_COMPOSED;
-    pp.ticketed = pp.staged || (sh.multi_dst_sum && pp.composed);
+    pp.composed = pol.ar_form == PL_AR_COMPOSED || pol.ar_form == PL_AR_NOTIFIED;
+    // Figure 6 without flags, zero-staging (every name of a reduction has R
+    // sources, so with several destinations every item reduces: the list
+    // needs no copy path).
+    pp.vector_compose = pol.ar_form == PL_AR_COMPOSED && !pp.staged && sh.multi_dst_sum;
+    pp.ticketed = pp.staged || (sh.multi_dst_sum && pp.composed && !pp.vector_compose);
     // Lists with flags that reduce (staged, composed) run the two-CTA kernels
     // even when aligned: their waits leave the single CTA's warps idle
     // (measured at 1 GiB: staged AllReduce 7.0 -> 5.9 ms, staged ReduceScatter
@@ -1194,6 +1199,23 @@ void Emitter::zero_staging(const Transfer& t, size_t row, const Chunk& ch)
 {
     const uint64_t blk = ch.nrows * ch.ncols * sh_.S;
     const bool sum = op_ != PL_COPY && t.srcs.size() > 1;  // a reduction (sum or maximum)
+    if (sum && t.dsts.size() > 1 && pp_.vector_compose) {
+        // Figure 6 at the grain of one vector: one item reduces the chunk
+        // into the owner's output (destination 0) and writes the others from
+        // there; each vector's reread follows its store in the same thread.
+        const size_t o = owner_of(t);
+        Builder::Pending cm;
+        for (auto& g : t.srcs)
+            cm.src.push_back(b.region(g, ch));
+        cm.dst.push_back(b.region(t.dsts[o], ch));
+        for (size_t d = 0; d < t.dsts.size(); ++d)
+            if (d != o)
+                cm.dst.push_back(b.region(t.dsts[d], ch));
+        put(row, 0, cm, kCompose, op_, ch);
+        bytes_read += blk * (t.srcs.size() + 1);
+        bytes_written += blk * t.dsts.size();
+        return;
+    }
     if (sum && t.dsts.size() > 1 && pp_.composed) {
         // Figure 6, zero-staging: the owner reduces the chunk into its output
         // and notifies; one item then reads the owner's chunk once and writes
@@ -1446,8 +1468,9 @@ pl_status finalise_plan(HostPlan& hp, const PlanShape& sh, const PlanPolicy& pp,
         hp.refs_per_item = uniform ? (int)n : 0;
     }
     hp.all_aligned = 1;
-    bool wide = true;
+    bool wide = true, compose = false;
     for (const Item& it : hp.items) {
+        compose |= it.kind == kCompose;
         if (it.op)
             wide &= it.nsrc >= 8;
         if (it.nsrc > kMaxRanks || it.ndst > kMaxRanks || it.nsrc == 0 || it.ndst == 0)
@@ -1466,6 +1489,8 @@ pl_status finalise_plan(HostPlan& hp, const PlanShape& sh, const PlanPolicy& pp,
         hp.ops |= kOpsWide;
     if (op == PL_MAX && (hp.ops & kOpsReduce))
         hp.ops |= kOpsMax;
+    if (compose)
+        hp.ops |= kOpsCompose;
     if (tickets && !waits_precede(hp))
         return PL_ERR_NOMEM;
 

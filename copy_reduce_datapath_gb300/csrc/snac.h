@@ -33,7 +33,7 @@ constexpr int kBulkMaxStages = 8;
 constexpr int kCtasPerSmAligned = 1;
 constexpr int kCtasPerSmSpliced = 2;
 
-enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2 };
+enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2, kCompose = 3 };
 enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3 };
 
 // Element types of a launch (the same codes as the public pl_dtype values).
@@ -48,9 +48,13 @@ constexpr int kOpsCopy = 1;
 constexpr int kOpsReduce = 2;  // items with several sources reduce them
 constexpr int kOpsWide = 4;    // every sum has at least 8 sources: one vector x 8 sources per step
 constexpr int kOpsMax = 8;     // the reduction is the maximum, not the sum
+// Every reduction with several destinations is a composed step (kCompose):
+// destination 0 receives the reduced values, the others are written from it.
+constexpr int kOpsCompose = 16;
 
 // One work item: move a rows x cols block from nsrc sources (copy if nsrc == 1,
-// rank-ordered reduction otherwise) into ndst destinations.  Refs
+// rank-ordered reduction otherwise) into ndst destinations (a kCompose item:
+// into destination 0, then from destination 0 into the others).  Refs
 // [ref, ref + nsrc) are sources, [ref + nsrc, ref + nsrc + ndst) destinations.
 // Syncs [sync, sync + nwait) run before the move, [sync + nwait, + npost) after.
 struct Item {

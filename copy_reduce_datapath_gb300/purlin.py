@@ -24,9 +24,9 @@ PL_ERR_NOMEM, PL_ERR_CUDA, PL_ERR_TIMEOUT, PL_ERR_UNSUPPORTED = 4, 5, 6, 7
 PL_COPY, PL_SUM, PL_MAX = 0, 1, 2
 PL_BF16, PL_FP32, PL_FP16, PL_FP8 = 0, 1, 2, 3
 PL_PATH_AUTO, PL_PATH_ZS, PL_PATH_STAGED = 0, 1, 2
-PL_AR_AUTO, PL_AR_FUSED, PL_AR_COMPOSED = 0, 1, 2
+PL_AR_AUTO, PL_AR_FUSED, PL_AR_COMPOSED, PL_AR_NOTIFIED = 0, 1, 2, 3
 PL_ATOM_AUTO, PL_ATOM_VECTOR, PL_ATOM_BULK, PL_ATOM_INLINE = 0, 1, 2, 3
-PL_ITEM_MOVE, PL_ITEM_STAGE, PL_ITEM_CONSUME = 0, 1, 2
+PL_ITEM_MOVE, PL_ITEM_STAGE, PL_ITEM_CONSUME, PL_ITEM_COMPOSE = 0, 1, 2, 3
 PL_SPACE_IN, PL_SPACE_OUT, PL_SPACE_SCRATCH = 0, 1, 2
 PL_SYNC_WAIT_FULL, PL_SYNC_WAIT_FREE, PL_SYNC_NOTIFY, PL_SYNC_CREDIT = 0, 1, 2, 3
 

@@ -93,7 +93,8 @@ typedef int32_t pl_dtype;
  * pl_policy_default() gives that.  A NULL policy pointer means all-auto. */
 typedef struct pl_policy {
     int32_t path;            /* PL_PATH_AUTO / PL_PATH_ZS / PL_PATH_STAGED */
-    int32_t allreduce_form;  /* PL_AR_AUTO / PL_AR_FUSED / PL_AR_COMPOSED (SUM with several outputs per name) */
+    int32_t allreduce_form;  /* PL_AR_AUTO / PL_AR_FUSED / PL_AR_COMPOSED / PL_AR_NOTIFIED (SUM or MAX with
+                                several outputs per name) */
     int32_t datapath;        /* PL_ATOM_AUTO / PL_ATOM_VECTOR / PL_ATOM_BULK / PL_ATOM_INLINE */
     int32_t ctas;            /* CTAs in the persistent grid; 0 = sized from the GPU's SM count and occupancy */
     int32_t stages;          /* depth of the bulk-copy shared-memory ring, 1..8; 0 = auto */
@@ -110,7 +111,14 @@ typedef struct pl_policy {
 
 #define PL_AR_AUTO      0 /* fused */
 #define PL_AR_FUSED     1 /* one work item reduces a chunk and writes it to every output of its name */
-#define PL_AR_COMPOSED  2 /* Figure 6: the owner reduces its partition's chunk, notifies, the others gather it */
+#define PL_AR_COMPOSED  2 /* Figure 6: the owner's reduce of its partition, then the gather of the reduced
+                             values from the owner's output to every other output.  Zero-staging composes
+                             at the grain of one 16-byte vector: the thread that stores a reduced vector
+                             into the owner's output reads it back from there and writes it to the other
+                             ranks, so program order takes the place of the Notify and the reread is served
+                             by L2.  The staged path composes per chunk with flags (as PL_AR_NOTIFIED). */
+#define PL_AR_NOTIFIED  3 /* Figure 6 per chunk: the owner's reduce item Notifies a flag; a separate gather
+                             item waits for it, reads the owner's chunk and writes the other ranks */
 
 #define PL_ATOM_AUTO    0 /* inline for plans that qualify (below) and either move at most 320 MiB or reduce
                              every name's sources into one destination (the ReduceScatter shape); else the bulk
@@ -235,7 +243,8 @@ PL_API pl_status pl_collective(pl_ctx* ctx, const pl_layout* in_layout, const pl
  * Figure 6): out_bufs[r][i] = rank-ordered sum over ranks of in_bufs[*][i]
  * for every r, by ReduceScatter then AllGather over R partitions (the first
  * R-1 of count/R elements, the last the rest).  policy->allreduce_form picks
- * the fused form (default) or the notified composed form of Figure 6.
+ * the fused form (default) or a composed form of Figure 6 (PL_AR_COMPOSED,
+ * PL_AR_NOTIFIED).
  * out_bufs may equal in_bufs (in place).  One kernel launch. */
 PL_API pl_status pl_allreduce(pl_ctx* ctx, pl_dtype dtype, int R, uint64_t count,
                               void* const* in_bufs, void* const* out_bufs,
@@ -312,6 +321,9 @@ typedef struct pl_plan_stats {
 #define PL_ITEM_MOVE     0 /* zero-staging Consume: sources -> destinations */
 #define PL_ITEM_STAGE    1 /* Stage: a source chunk -> a scratch slot, then Notify */
 #define PL_ITEM_CONSUME  2 /* Consume: wait for notified chunks, copy or reduce them into destinations */
+#define PL_ITEM_COMPOSE  3 /* zero-staging composed step (PL_AR_COMPOSED): reduce the sources into
+                              destination 0, the partition's owner; then read the reduced values back
+                              from destination 0 and write them to the other destinations */
 
 /* Spaces a region reference points into. */
 #define PL_SPACE_IN      0 /* in_bufs[index] */

@@ -88,6 +88,7 @@ def ar_policies():
     return {
         "zs_fused": P.pl_policy_default(),
         "zs_composed": P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=8192),
+        "zs_notified": P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED, chunk_bytes=8192),
         "staged_fused": P.pl_policy_default(path=P.PL_PATH_STAGED, chunk_bytes=8192),
         "staged_composed": P.pl_policy_default(path=P.PL_PATH_STAGED, allreduce_form=P.PL_AR_COMPOSED,
                                                chunk_bytes=8192),

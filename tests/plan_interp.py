@@ -93,7 +93,16 @@ def run(plan, R, dtype, ins, outs, *, window=1, seed=0):
         return _from_f32(dtype, acc)
 
     def write(it, refs, data):
-        for ref in refs[it.nsrc:]:
+        dsts = refs[it.nsrc:]
+        if it.kind == P.PL_ITEM_COMPOSE:
+            # Figure 6 at vector grain: destination 0 (the owner) first; the
+            # others receive what is read back from it
+            own = space[dsts[0].space][dsts[0].index]
+            idx = _index(dsts[0], it.rows, it.cols)
+            own[idx] = data
+            data = own[idx].copy()
+            dsts = dsts[1:]
+        for ref in dsts:
             buf = space[ref.space][ref.index]
             buf[_index(ref, it.rows, it.cols)] = data
 

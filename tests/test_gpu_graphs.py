@@ -29,6 +29,7 @@ def policies():
     return {
         "zs": None,
         "zs_composed": P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=8192),
+        "zs_notified": P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED, chunk_bytes=8192),
         "staged_fused": P.pl_policy_default(path=P.PL_PATH_STAGED, chunk_bytes=8192),
         "staged_composed": P.pl_policy_default(path=P.PL_PATH_STAGED, allreduce_form=P.PL_AR_COMPOSED,
                                                chunk_bytes=8192),

@@ -288,7 +288,8 @@ def test_repeated_calls_reuse_plans_and_flags(ctx):
     s = P.stream_handle()
     before = P.pl_ctx_launches(ctx)
     for i in range(6):
-        pol = list(ar_policies().values())[i % 4]
+        pols = list(ar_policies().values())
+        pol = pols[i % len(pols)]
         P.pl_allreduce(ctx, dtype, R, n, P.ptrs(dev), P.ptrs(outs), pol, s)
     assert P.pl_ctx_status(ctx, s) == P.PL_OK
     assert P.pl_ctx_launches(ctx) - before == 6
@@ -367,7 +368,7 @@ def test_bulk_shift_copy(ctx, dtype, stages):
         assert_equal(got[r], want[r], f"AGV rank {r}")
 
 
-@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
+@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED, P.PL_AR_NOTIFIED])
 def test_bulk_ring_in_flagged_paths(ctx, form):
     """Bulk copies inside staged and composed plans (stage, gather) with flags."""
     R, n, dtype = 8, 1 << 18, "bf16"

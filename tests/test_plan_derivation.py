@@ -89,7 +89,7 @@ def test_reducescatter_in_place(path, scratch):
 @pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("fp32", "sum"), ("fp16", "sum"), ("fp32", "max"),
                                       ("bf16", "max")])
 @pytest.mark.parametrize("path,scratch", PATHS)
-@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED])
+@pytest.mark.parametrize("form", [P.PL_AR_FUSED, P.PL_AR_COMPOSED, P.PL_AR_NOTIFIED])
 @pytest.mark.parametrize("window", WINDOWS)
 def test_allreduce(dtype, op, path, scratch, form, window):
     R = 3
@@ -232,13 +232,16 @@ def test_op_and_dtype_codes_are_checked():
 
 
 def test_reduction_items_name_their_op():
-    """Work items that reduce carry the op (1 sum, 2 maximum); copies carry 0."""
+    """Work items that reduce carry the op (1 sum, 2 maximum); copies carry 0:
+    the notified composed form's gathers copy, the vector-grain form's items
+    all reduce."""
     R = 4
     L = P.pl_layout_partitioned(R, [64] * R)
     for op, code in (("sum", 1), ("max", 2)):
-        pl = plan_for(L, L, op, "bf16", R, policy(P.PL_PATH_ZS, P.PL_AR_COMPOSED))
-        ops = {P.pl_plan_get_item(pl, i)[0].op for i in range(P.pl_plan_get_stats(pl).items)}
-        assert ops == {0, code}
+        for form, want in ((P.PL_AR_NOTIFIED, {0, code}), (P.PL_AR_COMPOSED, {code})):
+            pl = plan_for(L, L, op, "bf16", R, policy(P.PL_PATH_ZS, form))
+            ops = {P.pl_plan_get_item(pl, i)[0].op for i in range(P.pl_plan_get_stats(pl).items)}
+            assert ops == want
 
 
 def test_one_byte_chunks_and_alignment():
@@ -399,6 +402,9 @@ def test_inline_form_not_taken():
     assert form(*small_layouts("reducescatter", R, 1 << 29)) == P.PL_ATOM_INLINE    # 1 GiB: the ReduceScatter shape
     assert form(*ag, P.pl_policy_default(path=P.PL_PATH_STAGED)) == P.PL_ATOM_VECTOR
     assert form(*ar, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED)) == P.PL_ATOM_VECTOR
+    assert form(*ar, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, datapath=P.PL_ATOM_INLINE)) == \
+        P.PL_ATOM_VECTOR
+    assert form(*ar, P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED)) == P.PL_ATOM_VECTOR
     assert form(*ag, P.pl_policy_default(ctas=64)) == P.PL_ATOM_VECTOR
     assert form(*ag, P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)) == P.PL_ATOM_VECTOR
     assert form(*ag, P.pl_policy_default(datapath=P.PL_ATOM_BULK)) == P.PL_ATOM_BULK
@@ -440,9 +446,10 @@ def test_forced_inline_cuts_at_most_152_items():
 
 
 def test_flagged_reductions_take_two_ctas_per_sm():
-    """Lists with flags that reduce (staged, composed) are sized for the two-CTA
-    kernels even when aligned; staged copies and unflagged lists keep one CTA
-    per SM when aligned."""
+    """Lists with flags that reduce (staged, notified composed) are sized for
+    the two-CTA kernels even when aligned; staged copies and unflagged lists
+    (the vector-grain composed form among them) keep one CTA per SM when
+    aligned."""
     R, dtype, n = 8, "bf16", 1 << 22
     L = P.pl_layout_partitioned(R, [n // R] * R)
     lo = P.pl_layout_rank_owned(R, [n // R] * R)
@@ -456,16 +463,18 @@ def test_flagged_reductions_take_two_ctas_per_sm():
 
     staged = P.pl_policy_default(path=P.PL_PATH_STAGED)
     composed = P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED)
+    notified = P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED)
     vector = P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)
     assert ctas(L, L, "sum", staged) == 304
     assert ctas(L, lo, "sum", staged) == 304
-    assert ctas(L, L, "sum", composed) == 304
+    assert ctas(L, L, "sum", notified) == 304
+    assert ctas(L, L, "sum", composed) == 152
     assert ctas(lo, L, "copy", staged) == 152
     assert ctas(L, L, "sum", vector) == 152
 
 
-def test_composed_gather_reads_the_owners_chunk_once():
-    """Zero-staging composed AllReduce (Figure 6): per chunk, the owner's reduce
+def test_notified_gather_reads_the_owners_chunk_once():
+    """Zero-staging notified composed AllReduce (Figure 6): per chunk, the owner's reduce
     (R sources, one destination, then a Notify) and one gather item that waits
     for it and copies the reduced chunk to the R - 1 other ranks.  Bytes over
     all chunks: the reduces read R x n and write n elements, the gathers read n
@@ -473,7 +482,7 @@ def test_composed_gather_reads_the_owners_chunk_once():
     R, dtype, n = 8, "bf16", 8 * 3000 + 5
     ins = [rand(dtype, 73, r, n) for r in range(R)]
     L = P.pl_layout_partitioned(R, synth.equal_lengths(n, R))
-    pl = plan_for(L, L, "sum", dtype, R, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=1024))
+    pl = plan_for(L, L, "sum", dtype, R, P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED, chunk_bytes=1024))
     st, items = plan_interp.load_plan(pl)
     reduces = [(it, syncs) for it, _, syncs in items if it.nsrc == R]
     gathers = [(it, syncs) for it, _, syncs in items if it.nsrc == 1]
@@ -508,3 +517,38 @@ def test_one_to_one_plans_take_one_item_per_cta_up_to_512_kib():
     assert st.items == st.ctas and st.uses_tickets == 0
     st = stats(64 << 20)
     assert st.items > st.ctas and st.uses_tickets == 1
+
+
+@pytest.mark.parametrize("op", ["sum", "max"])
+@pytest.mark.parametrize("chunk", [0, 1024])
+def test_vector_grain_composition_writes_the_owner_first(op, chunk):
+    """Zero-staging PL_AR_COMPOSED (Figure 6 at the grain of one vector): one
+    kCompose item per chunk, no flags and no tickets; its first destination is
+    the output of the partition's owner (rank k for partition k), followed by
+    every other rank's output.  Bytes: the reduce reads R x n and writes n,
+    the reread reads n, the gather writes (R - 1) x n.  The emulator, which
+    writes the other ranks from what it reads back from the owner, gives the
+    oracle's result."""
+    R, dtype, n = 8, "bf16", 8 * 3000 + 5
+    ins = [rand(dtype, 74, r, n) for r in range(R)]
+    lens = synth.equal_lengths(n, R)
+    L = P.pl_layout_partitioned(R, lens)
+    pl = plan_for(L, L, op, dtype, R, P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED, chunk_bytes=chunk))
+    st, items = plan_interp.load_plan(pl)
+    assert st.syncs == 0 and st.flags == 0 and st.items == len(items) > 0
+    starts = np.cumsum([0] + lens)
+    for it, refs, syncs in items:
+        assert it.kind == P.PL_ITEM_COMPOSE and it.nsrc == R and it.ndst == R and not syncs
+        srcs, dsts = refs[:R], refs[R:]
+        assert [(f.space, f.index) for f in srcs] == [(P.PL_SPACE_IN, r) for r in range(R)]
+        owner = int(np.searchsorted(starts, srcs[0].offset, side="right")) - 1
+        assert (dsts[0].space, dsts[0].index) == (P.PL_SPACE_OUT, owner)
+        assert sorted(f.index for f in dsts[1:]) == [r for r in range(R) if r != owner]
+        assert all(f.offset == srcs[0].offset for f in refs)
+    S = 2
+    assert st.bytes_read == R * n * S + n * S
+    assert st.bytes_written == R * n * S
+    want = oracle.allreduce(ins, dtype, op=op)
+    outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=12)
+
