@@ -58,14 +58,19 @@ cudaError_t launch_inline(int dtype, bool maxop, const InlineSmall* small, const
     }
 }
 
-int snac_ctas_per_sm(bool aligned)
+int snac_ctas_per_sm(KernelClass k)
 {
     int n = 0;
+    constexpr int kMix = kOpsCopy | kOpsReduce, kWide = kOpsReduce | kOpsWide;
     const cudaError_t e =
-        aligned ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, true>,
-                                                                kThreads, 0)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kOpsCopy | kOpsReduce, false, false>,
-                                                                kThreadsSpliced, 0);
+        k == KernelClass::kAligned
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kMix, false, true>,
+                                                            snac_threads(kMix, true), 0)
+        : k == KernelClass::kAlignedReduce
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kWide, false, true>,
+                                                            snac_threads(kWide, true), 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, snac_kernel<kDtBf16, kMix, false, false>,
+                                                            snac_threads(kMix, false), 0);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;

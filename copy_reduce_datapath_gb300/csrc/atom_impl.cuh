@@ -1504,8 +1504,7 @@ __device__ __forceinline__ void item_loop_copy(const LaunchArgs& a, ItemShared* 
 // claims its next item only once its last claim returned an item of the list,
 // so every CTA makes exactly one claim beyond the end of the list.
 template <int DT, int OPS, bool BULK, bool ALIGN>
-__global__ void __launch_bounds__(ALIGN ? kThreads : OPS == kOpsCopy ? kThreadsSplicedCopy : kThreadsSpliced,
-                                  ALIGN ? kCtasPerSmAligned : kCtasPerSmSpliced)
+__global__ void __launch_bounds__(snac_threads(OPS, ALIGN), snac_min_ctas(OPS, ALIGN))
     snac_kernel(const __grid_constant__ LaunchArgs a, int stages)
 {
     __shared__ ItemShared sh[2];
@@ -1611,7 +1610,7 @@ cudaError_t launch_one(const LaunchArgs& args, int ctas, int stages, cudaStream_
             configured.fetch_or(bit, std::memory_order_acq_rel);
         }
     }
-    constexpr int threads = ALIGN ? kThreads : OPS == kOpsCopy ? kThreadsSplicedCopy : kThreadsSpliced;
+    constexpr int threads = snac_threads(OPS, ALIGN);
     snac_kernel<DT, OPS, BULK, ALIGN><<<ctas, threads, dyn, stream>>>(args, stages);
     return cudaGetLastError();
 }

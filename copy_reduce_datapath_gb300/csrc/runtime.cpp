@@ -90,6 +90,7 @@ uint64_t misaligned_cap(bool reduction, size_t ndst)
 // CTAs per SM of the SNAC kernels for aligned plans and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
+    int aligned_reduce = kCtasPerSmAlignedReduce;
     int spliced = kCtasPerSmSpliced;
 };
 constexpr size_t kMaxCachedPlans = 1024;
@@ -941,8 +942,10 @@ pl_status choose_policy(const PlanShape& sh, pl_op op, int R, const ResolvedPoli
     // each with its own CTAs per SM.  (The bulk ring's shared memory holds one
     // CTA per SM, whatever the kernel.)
     pp.flagged_reduction = pp.ticketed && op != PL_COPY;
-    pp.full_grid = std::max(1, num_sms) *
-                   std::max(1, (sh.regions_aligned || pp.bulk) && !pp.flagged_reduction ? occ.aligned : occ.spliced);
+    // (every item of a reduction over R > 1 ranks reduces: the reduce-only kernels)
+    const bool aligned_class = (sh.regions_aligned || pp.bulk) && !pp.flagged_reduction;
+    const int per_sm = !aligned_class ? occ.spliced : op != PL_COPY && R > 1 ? occ.aligned_reduce : occ.aligned;
+    pp.full_grid = std::max(1, num_sms) * std::max(1, per_sm);
     pp.grain = std::max<uint64_t>(E, kChunkGrain / S);
 
     uint64_t chunk_bytes = pol.chunk_bytes;
@@ -1519,7 +1522,8 @@ pl_status finalise_plan(HostPlan& hp, const PlanShape& sh, const PlanPolicy& pp,
     s.slots = pp.slots_per_rank;
     s.slot_elems = pp.staged ? pp.slot_elems : 0;
     s.ctas = hp.inline_form ? (int)hp.items.size() : ctas;
-    s.threads = hp.inline_form ? kInlineThreads : kThreads;
+    s.threads = hp.inline_form ? kInlineThreads
+                               : snac_threads(hp.ops, hp.all_aligned && !hp.flagged_reduction);
     s.uses_tickets = hp.inline_form ? 0 : (claim_in_order ? 1 : 0);
     s.path = pol.path;
     s.datapath = hp.inline_form ? PL_ATOM_INLINE : launch_bulk(hp, pol) ? PL_ATOM_BULK : PL_ATOM_VECTOR;
@@ -1943,9 +1947,13 @@ PL_API pl_status pl_ctx_create(pl_ctx** out, int device, uint64_t scratch_bytes)
     cudaError_t e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess)
         return cuda_fail(ctx.get(), e);
-    const int occ_aligned = snac_ctas_per_sm(true), occ_spliced = snac_ctas_per_sm(false);
+    const int occ_aligned = snac_ctas_per_sm(KernelClass::kAligned);
+    const int occ_aligned_reduce = snac_ctas_per_sm(KernelClass::kAlignedReduce);
+    const int occ_spliced = snac_ctas_per_sm(KernelClass::kSpliced);
     if (occ_aligned > 0)
         ctx->occ.aligned = std::min(occ_aligned, kCtasPerSmAligned);
+    if (occ_aligned_reduce > 0)
+        ctx->occ.aligned_reduce = std::min(occ_aligned_reduce, kCtasPerSmAlignedReduce);
     if (occ_spliced > 0)
         ctx->occ.spliced = std::min(occ_spliced, kCtasPerSmSpliced);
     pl_status st = ensure_flags(ctx.get(), 4096);

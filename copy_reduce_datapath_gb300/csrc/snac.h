@@ -32,6 +32,15 @@ constexpr int kBulkMaxStages = 8;
 // extra warps hide the splice and reduce arithmetic between memory waits.
 constexpr int kCtasPerSmAligned = 1;
 constexpr int kCtasPerSmSpliced = 2;
+// The kernels for aligned plans whose lists only reduce run two CTAs of 256
+// threads per SM at the same 128 registers: the same warps per SM in two
+// independently scheduled halves (measured on GB300, R = 8 bf16: the fused
+// AllReduce at 64 MiB 0.90 -> 0.93 of the roofline, at 128 MiB 0.946 ->
+// 0.958, at 1 GiB 0.987 -> 0.985; the composed one 0.898 -> 0.920, 0.935 ->
+// 0.947 and 0.972 -> 0.975).  Lists that copy keep one CTA of 512 (the bulk
+// ring's shared memory holds one CTA per SM).
+constexpr int kThreadsAlignedReduce = 256;
+constexpr int kCtasPerSmAlignedReduce = 2;
 
 enum ItemKind : uint8_t { kMove = 0, kStage = 1, kConsume = 2, kCompose = 3 };
 enum SyncType : uint8_t { kWaitFull = 0, kWaitFree = 1, kNotify = 2, kCredit = 3 };
@@ -51,6 +60,18 @@ constexpr int kOpsMax = 8;     // the reduction is the maximum, not the sum
 // Every reduction with several destinations is a composed step (kCompose):
 // destination 0 receives the reduced values, the others are written from it.
 constexpr int kOpsCompose = 16;
+
+// Threads per CTA, and CTAs per SM, of the kernel for an op mix and an
+// alignment class.
+constexpr int snac_threads(int ops, bool aligned)
+{
+    return aligned ? ((ops & kOpsCopy) ? kThreads : kThreadsAlignedReduce)
+                   : (ops == kOpsCopy ? kThreadsSplicedCopy : kThreadsSpliced);
+}
+constexpr int snac_min_ctas(int ops, bool aligned)
+{
+    return aligned ? ((ops & kOpsCopy) ? kCtasPerSmAligned : kCtasPerSmAlignedReduce) : kCtasPerSmSpliced;
+}
 
 // One work item: move a rows x cols block from nsrc sources (copy if nsrc == 1,
 // rank-ordered reduction otherwise) into ndst destinations (a kCompose item:
@@ -138,8 +159,10 @@ cudaError_t launch_snac_fp16(const LaunchArgs& a, int ctas, bool bulk, bool alig
 cudaError_t launch_snac_fp32(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
 cudaError_t launch_snac_fp8(const LaunchArgs& a, int ctas, bool bulk, bool aligned, int stages, cudaStream_t s);
 
-// CTAs of the SNAC kernel for aligned (or other) plans that fit on one SM at once.
-int snac_ctas_per_sm(bool aligned);
+// CTAs of the SNAC kernel that fit on one SM at once: for aligned plans whose
+// lists copy (kAligned) or only reduce (kAlignedReduce), and for other plans.
+enum class KernelClass { kAligned, kAlignedReduce, kSpliced };
+int snac_ctas_per_sm(KernelClass k);
 
 // ------------------------------------------------- inline-parameter launches
 //

@@ -447,17 +447,19 @@ def test_forced_inline_cuts_at_most_152_items():
 
 def test_flagged_reductions_take_two_ctas_per_sm():
     """Lists with flags that reduce (staged, notified composed) are sized for
-    the two-CTA kernels even when aligned; staged copies and unflagged lists
-    (the vector-grain composed form among them) keep one CTA per SM when
-    aligned."""
+    the two-CTA spliced kernels (512 threads) even when aligned; aligned lists
+    without flags that only reduce (the fused and vector-grain composed
+    AllReduce) for two CTAs of 256 threads per SM; staged copies and aligned
+    copies keep one CTA of 512 per SM."""
     R, dtype, n = 8, "bf16", 1 << 22
     L = P.pl_layout_partitioned(R, [n // R] * R)
     lo = P.pl_layout_rank_owned(R, [n // R] * R)
 
-    def ctas(lin, lout, op, pol):
+    def shape(lin, lout, op, pol):
         pl = P.pl_plan_create(lin, lout, op, dtype, R, pol, num_sms=152, scratch_bytes=64 << 20)
         try:
-            return P.pl_plan_get_stats(pl).ctas
+            st = P.pl_plan_get_stats(pl)
+            return st.ctas, st.threads
         finally:
             P.pl_plan_destroy(pl)
 
@@ -465,12 +467,13 @@ def test_flagged_reductions_take_two_ctas_per_sm():
     composed = P.pl_policy_default(allreduce_form=P.PL_AR_COMPOSED)
     notified = P.pl_policy_default(allreduce_form=P.PL_AR_NOTIFIED)
     vector = P.pl_policy_default(datapath=P.PL_ATOM_VECTOR)
-    assert ctas(L, L, "sum", staged) == 304
-    assert ctas(L, lo, "sum", staged) == 304
-    assert ctas(L, L, "sum", notified) == 304
-    assert ctas(L, L, "sum", composed) == 152
-    assert ctas(lo, L, "copy", staged) == 152
-    assert ctas(L, L, "sum", vector) == 152
+    assert shape(L, L, "sum", staged) == (304, 512)
+    assert shape(L, lo, "sum", staged) == (304, 512)
+    assert shape(L, L, "sum", notified) == (304, 512)
+    assert shape(L, L, "sum", composed) == (304, 256)
+    assert shape(L, L, "sum", vector) == (304, 256)
+    assert shape(lo, L, "copy", staged) == (152, 512)
+    assert shape(lo, L, "copy", vector) == (152, 512)
 
 
 def test_notified_gather_reads_the_owners_chunk_once():
