@@ -58,6 +58,12 @@ constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA
 // AllToAllV of 16 MiB per rank, 431 KB per CTA, 63.3 us guided, 54.5 us with
 // chunks of 512 KiB; at 64 MiB and more the guided chunks stay best)
 constexpr uint64_t kOneItemBytesOneToOne = 512 << 10;
+// ... and for the ReduceScatter shape between regions not all 16-byte aligned
+// (the ReduceScatterV), whose realigning reduction runs best in one item per
+// CTA (measured on GB300, Zipf lengths, R = 8 bf16, guided against one item
+// per CTA: 128 MiB per rank 0.84 -> 0.92-0.94 of the roofline, 256 MiB
+// 0.89 -> 0.94-0.97; with 2 MiB the 512 MiB point lost 0.953 -> 0.945)
+constexpr uint64_t kOneItemBytesScatterMisaligned = 1 << 20;
 constexpr uint64_t kChunkGrain = 256;           // automatic chunk sizes are multiples of this many bytes
 constexpr uint64_t kBulkItemBytes = 512 << 10;  // bytes (read + written) of an automatic bulk-ring item
 constexpr uint64_t kBulkChunkMin = 64 << 10;    // ... whose chunk stays within these
@@ -863,11 +869,13 @@ void share_targets(const PlanShape& sh, uint64_t grain, uint64_t min_elems, Shar
 // The automatic chunk rule of a zero-staging list whose items never wait on
 // one another.  A CTA moves its items one after another and each item starts
 // with a memory round trip that nothing overlaps, so:
-//  - small messages (at most kOneItemBytes per CTA) get about one item per
+//  - small messages (at most kOneItemBytes per CTA; more for one-to-one
+//    transfers and for misaligned ReduceScatters) get about one item per
 //    CTA: each transfer is cut into its share of the grid;
-//  - larger ones whose transfers all have one size and fan-out, and aligned
-//    ones the bulk ring moves, are cut into k near-equal items per CTA (k =
-//    kItemsPerCta, or enough to keep chunks within the cap);
+//  - larger ones whose transfers all have one size and fan-out, and those
+//    the bulk ring moves (aligned, or realigned in shared memory), are cut
+//    into k near-equal items per CTA (k = kItemsPerCta, or enough to keep
+//    chunks within the cap);
 //  - the others are cut by guided self-scheduling: each next item moves about
 //    remaining bytes / (kGuidedDiv x grid), so items shrink toward the end of
 //    the list, and CTAs that claim them in order as they finish end within one
@@ -886,7 +894,10 @@ void choose_auto_rule(const PlanShape& sh, pl_op op, const ResolvedPolicy& pol, 
         pp.rule = ChunkRule::kInline;
         return;
     }
-    if (sh.total_bytes / grid <= (sh.one_to_one ? kOneItemBytesOneToOne : kOneItemBytes)) {
+    const uint64_t one_item = sh.one_to_one                         ? kOneItemBytesOneToOne
+                              : sh.rs_shape && !sh.regions_aligned ? kOneItemBytesScatterMisaligned
+                                                                   : kOneItemBytes;
+    if (sh.total_bytes / grid <= one_item) {
         pp.rule = ChunkRule::kPerCta;
         const uint64_t min_elems = std::max(pp.grain, kMinChunkBytes / S / pp.grain * pp.grain);
         share_targets(sh, pp.grain, min_elems, [&](const Transfer& t) {
@@ -894,16 +905,19 @@ void choose_auto_rule(const PlanShape& sh, pl_op op, const ResolvedPolicy& pol, 
         }, pp.target);
         return;
     }
-    if (sh.equal || (pp.bulk && sh.all_aligned_regions)) {
+    if (sh.equal || pp.bulk) {
         // k items per CTA, each transfer cut into floor(its share of k x grid)
         // near-equal chunks: at most k items per CTA, none much larger than
         // total / (k x grid).  On the bulk ring an item moves about
         // kBulkItemBytes (measured on GB300: an AllGather at 1 GiB, one source
         // and eight destinations, best with 64 KiB chunks; the MoE AllToAll,
-        // one and one, with 256 KiB).
+        // one and one, with 256 KiB; the Zipf AllGatherV, whose sources the
+        // ring realigns, with 64 KiB chunks from 64 MiB per rank up: 0.81 ->
+        // 0.87 of the roofline at 64 MiB, 0.82 -> 0.93 at 128 MiB, 0.94 ->
+        // 0.98 at 1 GiB, against guided items).
         pp.rule = ChunkRule::kEqual;
         const uint64_t bulk_chunk = std::min(std::max(kBulkItemBytes / sh.fanout, kBulkChunkMin), kBulkChunkMax);
-        const uint64_t cap = pp.bulk && sh.all_aligned_regions ? bulk_chunk : kMaxChunkBytes;
+        const uint64_t cap = pp.bulk ? bulk_chunk : kMaxChunkBytes;
         const uint64_t per_cta = (sh.total_bytes + grid - 1) / grid;
         const uint64_t k = std::max<uint64_t>((per_cta + cap - 1) / cap, kItemsPerCta);
         const uint64_t items = k * grid;

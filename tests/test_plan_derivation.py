@@ -261,10 +261,9 @@ def test_one_byte_chunks_and_alignment():
 def test_automatic_chunking_covers_every_element(kind, scale):
     """Automatic chunks of plans whose items never wait (zero-staging), on a
     4-SM grid: about one item per CTA for small messages (scale 1: under
-    256 KiB per CTA); for larger ones (scale 20) one large item per CTA and a
-    few small ones after it (the V forms), or guided sizes that shrink along
-    the list (strided rows), claimed in order once there are more items than
-    CTAs.
+    256 KiB per CTA, and the misaligned ReduceScatterV up to 1 MiB per CTA,
+    so at both scales); for larger ones (scale 20) guided sizes that shrink
+    along the list, claimed in order once there are more items than CTAs.
     Executed by the emulator, the result equals the oracle.  (The vector
     datapath: the persistent kernel's chunk rule, not the inline form's.)"""
     R, dtype = 8, "bf16"
@@ -299,7 +298,9 @@ def test_automatic_chunking_covers_every_element(kind, scale):
     st, items = plan_interp.load_plan(pl)
     sizes = [it.rows * it.cols for it, _, _ in items]
     assert st.uses_tickets == (1 if st.items > st.ctas else 0)
-    if scale > 1 and kind != "alltoallv":  # (64 short transfers on 4 SMs: one item each, in turn)
+    if kind == "reducescatterv":
+        assert st.items <= st.ctas and st.uses_tickets == 0
+    elif scale > 1 and kind != "alltoallv":  # (64 short transfers on 4 SMs: one item each, in turn)
         assert st.items > st.ctas
         assert max(sizes) <= 2 * sizes[0]  # the list starts with its largest items
         assert sum(sizes[: len(sizes) // 4]) >= sum(sizes[-(len(sizes) // 4):])  # and ends with small ones
