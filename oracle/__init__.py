@@ -241,6 +241,14 @@ class Oracle:
             arr = (_Part * max(1, len(items)))(*items)
             return counts, arr
 
+        # every part inside its buffer (the C code takes bare pointers)
+        for layout, sizes in ((in_layout, [a.size for a in ins]), (out_layout, [int(s) for s in out_sizes])):
+            for parts, size in zip(layout, sizes):
+                for p in parts:
+                    p = tuple(int(v) for v in p)
+                    rows, stride = (p[3], p[4]) if len(p) == 5 else (1, p[2])
+                    if p[2] and p[1] + (rows - 1) * stride + p[2] > size:
+                        raise ValueError("a layout part lies outside its buffer")
         nin, pin = flat(in_layout)
         nout, pout = flat(out_layout)
         outs = [np.zeros(int(s), dtype=npdt) for s in out_sizes]
