@@ -93,7 +93,8 @@ uint64_t misaligned_cap(bool reduction, size_t ndst)
     return reduction ? kInlineMisalignedReduceVectors : ndst == 1 ? kInlineMisalignedOneDstVectors
                                                                   : kInlineMisalignedCopyVectors;
 }
-// CTAs per SM of the SNAC kernels for aligned plans and for other plans.
+// CTAs per SM of the SNAC kernels for aligned plans that copy, for aligned
+// plans that only reduce, and for other plans.
 struct Occupancy {
     int aligned = kCtasPerSmAligned;
     int aligned_reduce = kCtasPerSmAlignedReduce;
