@@ -53,6 +53,7 @@ constexpr int kGuidedTailMovedDiv = 16;
 // AllGatherV 0.71 -> 0.75, ReduceScatterV 0.77 -> 0.84, AllToAllV 0.82 ->
 // 0.85 of the roofline; from 256 MiB per rank the finer start wins).
 constexpr uint64_t kGuidedCoarseMoved = 1536ull << 20;
+constexpr uint64_t kGuidedRowsTailFloor = 128 << 10;  // see cut_guided_rows
 constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA: one item per CTA
 // ... and for plans of one-to-one transfers (the AllToAll shape; measured: the
 // AllToAllV of 16 MiB per rank, 431 KB per CTA, 63.3 us guided, 54.5 us with
@@ -1071,9 +1072,18 @@ void cut_guided_rows(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
         rem_moved += rem[i] * w[i];
     }
     // The smallest rows: total / (kGuidedTailDiv x grid), from kMinChunkBytes (a
-    // small message still gets several items per CTA) to kGuidedTailMax.
+    // small message still gets several items per CTA) to kGuidedTailMax; and
+    // at least total / (2 x grid) up to kGuidedRowsTailFloor, so that smaller
+    // messages end in fewer, larger rows: each item of these lists waits on a
+    // flag or posts one, and small items paid that cost too often (measured on
+    // GB300, the notified AllReduce at 16 / 64 / 128 / 256 MiB / 1 GiB per
+    // rank: 0.34 / 0.60 / 0.73 / 0.83 / 0.89 of the roofline with the plain
+    // tail, 0.50 / 0.73 / 0.79 / 0.84 / 0.89 with this floor; a tail of
+    // total / (2 x grid) up to 1 MiB cost the 1 GiB point 0.89 -> 0.86).
     const uint64_t tail_bytes =
-        std::min(std::max(sh.total_bytes / (grid * kGuidedTailDiv), kMinChunkBytes), kGuidedTailMax);
+        std::min(std::max({sh.total_bytes / (grid * kGuidedTailDiv),
+                           std::min(sh.total_bytes / (grid * 2), kGuidedRowsTailFloor), kMinChunkBytes}),
+                 kGuidedTailMax);
     const uint64_t min_elems = round_grain(tail_bytes / S);
     const uint64_t max_elems = round_grain(kMaxChunkBytes / S);
     while (rem_moved > 0) {
