@@ -114,17 +114,3 @@ def policy(P, name):
         "few_ctas": P.pl_policy_default(ctas=3),
     }[name]
 
-
-def named_mask(layout, sizes):
-    """Per rank, a boolean list marking the output elements some part names."""
-    masks = []
-    for parts, n in zip(layout, sizes):
-        mk = [False] * n
-        for p in parts:
-            _, off, ln = p[0], p[1], p[2]
-            rows, stride = (p[3], p[4]) if len(p) == 5 else (1, ln)
-            for r in range(rows):
-                for c in range(ln):
-                    mk[off + r * stride + c] = True
-        masks.append(mk)
-    return masks
