@@ -133,3 +133,18 @@ def test_composed_allreduce_1GiB(ctx):
         del wl
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("form", list(FORMS))
+def test_composed_allreduce_64_ranks(ctx, form):
+    """R = 64, the most sources and destinations an item holds: the owner first
+    among 64 destinations, outputs aligned and misaligned."""
+    R, dtype = 64, "bf16"
+    lens = [8 * 37] * R
+    n = sum(lens)
+    ins = [host("normal", dtype, 84, r, n) for r in range(R)]
+    L = P.pl_layout_partitioned(R, lens)
+    got = run(ctx, L, L, "sum", dtype, ins, [n] * R, P.pl_policy_default(allreduce_form=FORMS[form]))
+    want = oracle.allreduce(ins, dtype)
+    for r in range(R):
+        assert_equal(got[r], want[r], f"rank {r}")
