@@ -59,6 +59,11 @@ constexpr uint64_t kOneItemBytes = 256 << 10;   // up to this many bytes per CTA
 // AllToAllV of 16 MiB per rank, 431 KB per CTA, 63.3 us guided, 54.5 us with
 // chunks of 512 KiB; at 64 MiB and more the guided chunks stay best)
 constexpr uint64_t kOneItemBytesOneToOne = 512 << 10;
+// ... up to 2 MiB when those transfers are not all 16-byte aligned (the
+// AllToAllV, realigned by the spliced copy kernel; measured on GB300: 32 MiB
+// per rank 0.76 -> 0.80 of the roofline, 64 MiB 0.86 -> 0.87, 128 MiB and
+// more unchanged; the aligned AllToAll lost with it, 0.88 -> 0.81 at 32 MiB)
+constexpr uint64_t kOneItemBytesOneToOneMisaligned = 2 << 20;
 // ... and for the ReduceScatter shape between regions not all 16-byte aligned
 // (the ReduceScatterV), whose realigning reduction runs best in one item per
 // CTA (measured on GB300, Zipf lengths, R = 8 bf16, guided against one item
@@ -896,7 +901,7 @@ void choose_auto_rule(const PlanShape& sh, pl_op op, const ResolvedPolicy& pol, 
         pp.rule = ChunkRule::kInline;
         return;
     }
-    const uint64_t one_item = sh.one_to_one                         ? kOneItemBytesOneToOne
+    const uint64_t one_item = sh.one_to_one ? (sh.regions_aligned ? kOneItemBytesOneToOne : kOneItemBytesOneToOneMisaligned)
                               : sh.rs_shape && !sh.regions_aligned ? kOneItemBytesScatterMisaligned
                                                                    : kOneItemBytes;
     if (sh.total_bytes / grid <= one_item) {

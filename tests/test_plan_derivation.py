@@ -501,26 +501,35 @@ def test_notified_gather_reads_the_owners_chunk_once():
     run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=11)
 
 
-def test_one_to_one_plans_take_one_item_per_cta_up_to_512_kib():
-    """An AllToAllV of 16 MiB per rank (about 431 KB per CTA of a 304-CTA grid):
-    one item per CTA, no ticket; at 64 MiB per rank, guided items claimed in
-    order."""
+def test_one_to_one_plans_take_one_item_per_cta():
+    """One-to-one transfers take one item per CTA up to 512 KiB per CTA when
+    aligned and up to 2 MiB when not: an AllToAllV (Zipf rows, misaligned) of
+    64 MiB per rank (about 1.8 MB per CTA of a 304-CTA grid) runs one item per
+    CTA with no ticket, of 128 MiB guided items claimed in order; the aligned
+    AllToAll of 32 MiB per rank (1.8 MB per CTA of 152) near-equal items."""
     R = 8
 
-    def stats(T):
-        N = T // 2
-        m = synth.zipf_matrix(N, R, 0.125, seed=4)
-        pl = P.pl_plan_create(P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m), "copy", "bf16", R,
-                              P.pl_policy_default(datapath=P.PL_ATOM_VECTOR), num_sms=152)
+    def stats(lin, lout):
+        pl = P.pl_plan_create(lin, lout, "copy", "bf16", R, P.pl_policy_default(datapath=P.PL_ATOM_VECTOR),
+                              num_sms=152)
         try:
             return P.pl_plan_get_stats(pl)
         finally:
             P.pl_plan_destroy(pl)
 
-    st = stats(16 << 20)
+    def a2av(T):
+        m = synth.zipf_matrix(T // 2, R, 0.125, seed=4)
+        return stats(P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m))
+
+    st = a2av(16 << 20)
     assert st.items == st.ctas and st.uses_tickets == 0
-    st = stats(64 << 20)
+    st = a2av(64 << 20)
+    assert st.items <= st.ctas and st.uses_tickets == 0
+    st = a2av(128 << 20)
     assert st.items > st.ctas and st.uses_tickets == 1
+    m = [[(32 << 20) // 2 // R] * R for _ in range(R)]
+    st = stats(P.pl_layout_alltoall_in(R, m), P.pl_layout_alltoall_out(R, m))
+    assert st.items > st.ctas
 
 
 @pytest.mark.parametrize("op", ["sum", "max"])
