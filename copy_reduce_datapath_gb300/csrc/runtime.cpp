@@ -1112,6 +1112,30 @@ void cut_guided_rows(const PlanShape& sh, const PlanPolicy& pp, Cuts& cu)
     }
 }
 
+// The last `m` chunks of one transfer (at most half of them) cut in two, in
+// multiples of the grain: a list of equal items on the bulk ring then ends
+// with about two grids of half-size items, so that the CTAs, which run at
+// different rates, finish within half an item of each other instead of a
+// whole one (measured on GB300, R = 8 bf16: AllGather 0.87 -> 0.89 of the
+// roofline at 64 MiB per rank, 0.93 -> 0.95 at 128 MiB; AllToAll 0.94 ->
+// 0.95 and 0.986 -> 0.996; MoE AllToAll 147 -> 145 us; cutting the last
+// three grids, or into quarters, gained less).
+void halve_last_chunks(std::vector<Chunk>& chunks, size_t m, uint64_t grain)
+{
+    m = std::min(m, chunks.size() / 2);
+    std::vector<Chunk> tail(chunks.end() - (std::ptrdiff_t)m, chunks.end());
+    chunks.resize(chunks.size() - m);
+    for (const Chunk& c : tail) {
+        if (c.nrows != 1) {
+            chunks.push_back(c);
+            continue;
+        }
+        const uint64_t half = std::max(grain, ((c.ncols + 1) / 2 + grain - 1) / grain * grain);
+        for (uint64_t c0 = 0; c0 < c.ncols; c0 += half)
+            chunks.push_back(Chunk{c.row0, 1, c.col0 + c0, std::min(half, c.ncols - c0)});
+    }
+}
+
 Cuts cut_chunks(const PlanShape& sh, const PlanPolicy& pp)
 {
     Cuts cu;
@@ -1132,6 +1156,9 @@ Cuts cut_chunks(const PlanShape& sh, const PlanPolicy& pp)
                 cu.chunks[i].push_back(ch);
                 left -= ch.nrows * ch.ncols;
             }
+            if (pp.rule == ChunkRule::kEqual && pp.bulk && sh.equal)
+                halve_last_chunks(cu.chunks[i], (2 * (size_t)pp.full_grid + sh.ts.size() - 1) / sh.ts.size(),
+                                  pp.grain);
         }
     }
     for (auto& cs : cu.chunks)
