@@ -134,7 +134,7 @@ typedef struct pl_policy {
                              plans of one-row regions at 16-byte aligned offsets whose items (at most 152) and
                              references (at most 2432) fit the parameter block.  Buffers not 16-byte aligned at
                              launch, and plans that do not qualify, run the same work list on the vector (or bulk)
-                             datapath. */
+                             datapath; so do lists with flags and the zero-staging PL_AR_COMPOSED form. */
 
 /* Fills *pol with the all-auto policy (debug_drop_notify = -1). */
 PL_API void pl_policy_default(pl_policy* pol);
