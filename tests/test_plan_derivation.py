@@ -565,3 +565,22 @@ def test_vector_grain_composition_writes_the_owner_first(op, chunk):
     outs = [np.zeros(n, NP[dtype]) for _ in range(R)]
     run_and_check(pl, R, dtype, ins, outs, want, window=8, seed=12)
 
+
+
+def test_equal_bulk_lists_end_with_half_size_items():
+    """An AllGather on the bulk ring (equal transfers): near-equal items, then
+    about two grids of half-size items at the end of the list; every element
+    covered once, and the emulator gives the oracle's result."""
+    R, dtype = 8, "bf16"
+    n = 1 << 19  # 1 MiB per rank: 2 MiB per CTA of a 4-SM grid
+    lin, lout, op = P.pl_layout_rank_owned(R, [n] * R), P.pl_layout_partitioned(R, [n] * R), "copy"
+    pl = plan_for(lin, lout, op, dtype, R, P.pl_policy_default(datapath=P.PL_ATOM_BULK))
+    st, items = plan_interp.load_plan(pl)
+    sizes = [it.cols for it, _, _ in items]
+    assert st.datapath == P.PL_ATOM_BULK and sum(sizes) == R * n
+    tail = 2 * st.ctas
+    assert max(sizes[-tail:]) * 2 <= max(sizes[:-tail]) + 128  # halves (grain-rounded) of the equal items
+    ins = [rand(dtype, 75, r, n) for r in range(R)]
+    want = oracle.allgather(ins, dtype)
+    outs = [np.zeros(n * R, NP[dtype]) for _ in range(R)]
+    run_and_check(pl, R, dtype, ins, outs, want, window=6, seed=13)
